@@ -1,0 +1,215 @@
+"""Seeded synthetic inputs for the sparse MLA prefill forward.
+
+This module builds the tensors both sides of a parity check consume: the
+bf16 query and KV pool (as raw bf16 bit patterns), the per-head fp32 attention
+sink, and the ``[T, TOPK]`` index lists.  It holds none of the method's
+arithmetic (no scores, no softmax, no validity rule): only random numbers,
+bf16 rounding of those numbers and the index-list layout.
+
+Index-list recipe.  The pages measure on captured engine inputs that are not
+available; the backward PR ("Sparse MLA training backward", section
+"Performance") says the realistic top-k is a sliding window plus a causally
+visible compressed pool, not uniform random.  Each token's list is laid out as
+``[window segment | pool segment]``:
+
+* window segment (``W`` slots): token rows ``t-W+1 .. t`` ascending, the token
+  itself last; a row below 0 is written as ``-1`` (early tokens carry ``-1``
+  inside the row, as the serving engine does);
+* pool segment (``TOPK - W`` slots): pool row ``p`` (stored at kv row
+  ``T + p``) is visible to token ``t`` iff ``ratio*(p+1) <= t+1``.  All visible
+  rows are taken when they fit, otherwise a seeded sample without replacement,
+  sorted ascending; ``-1`` fills the rest.
+
+The valid count depends only on visibility, so FLOPs and bytes are fixed by
+the configuration, whatever the sample.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+D = 512
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    """One synthetic workload.
+
+    ``num_kv = T + pool``: kv rows ``0..T-1`` are per-token rows and
+    ``T..num_kv-1`` the compressed pool (kv layout of the "Contract" section of
+    "Sparse MLA training backward").
+    """
+
+    name: str
+    T: int
+    H: int
+    pool: int
+    ratio: int
+    topk: int
+    window: int
+    index_dtype: str = "int32"  # "int32" | "int64"
+    sink: bool = True
+    kv_offset_bytes: int = 0  # where kv starts inside its device allocation
+    seed: int = 0
+
+    @property
+    def num_kv(self) -> int:
+        return self.T + self.pool
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(D))
+
+    def with_(self, **kw) -> "Config":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads (seeds 0..4 in this order).  Shapes follow the pages:
+# H=8/16 is the DSv4.1-Flash TP4 per-rank head count with 32..640 slots
+# ("Tuned sparse MLA prefill for DSv4.1-Flash TP4", description "Perf");
+# T=4096/8192, H=128, topk 512/1024 are the backward's measured shapes
+# ("Sparse MLA training backward", section "Performance").
+CONFIGS = {
+    "tiny": Config("tiny", T=64, H=16, pool=16, ratio=4, topk=64, window=32, seed=0),
+    "small_head": Config("small_head", T=16384, H=16, pool=4096, ratio=4, topk=640,
+                         window=128, seed=1),
+    "sweep_k32": Config("sweep_k32", T=4096, H=8, pool=1024, ratio=4, topk=32, window=32, seed=2),
+    "sweep_k128": Config("sweep_k128", T=4096, H=8, pool=1024, ratio=4, topk=128, window=128,
+                         seed=2),
+    "sweep_k256": Config("sweep_k256", T=4096, H=8, pool=1024, ratio=4, topk=256, window=128,
+                         seed=2),
+    "sweep_k640": Config("sweep_k640", T=4096, H=8, pool=1024, ratio=4, topk=640, window=128,
+                         seed=2),
+    "sweep_k640_nosink": Config("sweep_k640_nosink", T=4096, H=8, pool=1024, ratio=4, topk=640,
+                                window=128, sink=False, seed=2),
+    "h128": Config("h128", T=4096, H=128, pool=1024, ratio=4, topk=512, window=128, seed=3),
+    "h128_long": Config("h128_long", T=8192, H=128, pool=1024, ratio=8, topk=1024, window=256,
+                        index_dtype="int64", kv_offset_bytes=(2 << 30) + 4096, seed=4),
+}
+
+# The workload the headline metric is quoted on (T=4096 H=128 topk=512).
+BENCH_CONFIG = "h128"
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even); returns uint16 bits.
+
+    Inputs are finite N(0,1) draws; no NaN handling is needed or attempted.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 (exact)."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _normal_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
+    """N(0,1) draws rounded to bf16, generated in fixed-size chunks."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        out[s:e] = bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+    return out.reshape(shape)
+
+
+def make_indices(cfg: Config, rng: np.random.Generator) -> np.ndarray:
+    """``[T, TOPK]`` index lists per the window + causally visible pool recipe."""
+    T, K, W = cfg.T, cfg.topk, cfg.window
+    if W > K:
+        raise ValueError("window larger than TOPK")
+    dt = np.int64 if cfg.index_dtype == "int64" else np.int32
+    idx = np.full((T, K), -1, dtype=np.int64)
+    t = np.arange(T, dtype=np.int64)
+    # window segment: rows t-W+1 .. t, -1 below 0
+    win = t[:, None] - (W - 1) + np.arange(W, dtype=np.int64)[None, :]
+    win[win < 0] = -1
+    idx[:, :W] = win
+    kp = K - W
+    if kp > 0 and cfg.pool > 0:
+        vis = np.minimum(cfg.pool, (t + 1) // cfg.ratio)  # visible pool rows per token
+        full = vis <= kp
+        # tokens whose visible pool fits: take all visible rows in order
+        ar = np.arange(kp, dtype=np.int64)[None, :]
+        take = np.where(ar < vis[:, None], cfg.T + ar, -1)
+        idx[full, W:] = take[full]
+        # tokens with more visible rows than pool slots: seeded sample, sorted
+        need = np.nonzero(~full)[0]
+        chunk = 512
+        for s in range(0, len(need), chunk):
+            rows = need[s:s + chunk]
+            keys = rng.random((len(rows), cfg.pool))
+            pcol = np.arange(cfg.pool, dtype=np.int64)[None, :]
+            keys[pcol >= vis[rows][:, None]] = np.inf
+            pick = np.argpartition(keys, kp - 1, axis=1)[:, :kp]
+            pick.sort(axis=1)
+            idx[rows, W:] = cfg.T + pick
+    return idx.astype(dt)
+
+
+def make_inputs(cfg: Config) -> dict:
+    """All inputs of one workload, as host numpy arrays.
+
+    Returns a dict with ``q`` (uint16 bf16 bits ``[T,H,512]``), ``kv`` (uint16
+    bf16 bits ``[num_kv,512]``), ``idx`` (int32/int64 ``[T,TOPK]``), ``sink``
+    (float32 ``[H]`` or None) and ``scale``.
+    """
+    rng = np.random.Generator(np.random.PCG64(cfg.seed))
+    q = _normal_bf16(rng, (cfg.T, cfg.H, D))
+    kv = _normal_bf16(rng, (cfg.num_kv, D))
+    sink = rng.standard_normal(cfg.H, dtype=np.float32)
+    idx = make_indices(cfg, rng)
+    return {"q": q, "kv": kv, "idx": idx, "sink": sink if cfg.sink else None,
+            "scale": cfg.scale}
+
+
+# ---------------------------------------------------------------- test variants
+def shuffle_rows(idx: np.ndarray, seed: int) -> np.ndarray:
+    """Permute every token's slot list independently (seeded)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    keys = rng.random(idx.shape)
+    order = np.argsort(keys, axis=1)
+    return np.take_along_axis(idx, order, axis=1)
+
+
+def inject_out_of_range(idx: np.ndarray, num_kv: int, seed: int, frac: float = 0.1,
+                        values: Optional[list] = None) -> np.ndarray:
+    """Overwrite a seeded fraction of slots with values outside ``[0, num_kv)``.
+
+    Default values: -1, num_kv (first row past the pool), a value far past it
+    and the int32 maximum; int64 lists also get 2**31, 2**32 + 3 and -2**40
+    (values that would wrap onto valid rows if narrowed to int32).
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if values is None:
+        values = [-1, num_kv, num_kv + 12345, np.iinfo(np.int32).max, -7]
+        if idx.dtype == np.int64:
+            values += [2 ** 31, 2 ** 32 + 3, -(2 ** 40), 2 ** 31 + 1]
+    out = idx.copy()
+    hit = rng.random(idx.shape) < frac
+    pick = rng.integers(0, len(values), size=idx.shape)
+    vals = np.asarray(values, dtype=np.int64)[pick].astype(idx.dtype)
+    out[hit] = vals[hit]
+    return out
+
+
+def inject_duplicates(idx: np.ndarray, num_kv: int, seed: int, frac: float = 0.1) -> np.ndarray:
+    """Copy a seeded fraction of valid slots over other slots of the same token."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = idx.copy()
+    T, K = idx.shape
+    for t in range(T):
+        row = out[t]
+        valid = np.nonzero((row >= 0) & (row < num_kv))[0]
+        if len(valid) == 0:
+            continue
+        n = max(1, int(frac * K))
+        dst = rng.integers(0, K, size=n)
+        src = valid[rng.integers(0, len(valid), size=n)]
+        row[dst] = row[src]
+    return out
