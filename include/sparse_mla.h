@@ -1,0 +1,136 @@
+/*
+ * sparse_mla.h -- C ABI of the GB300 (sm_103a) sparse MLA prefill forward.
+ *
+ * The operation (DeepSeek-V4 sparse MLA, "has_pe = False" path) is the one
+ * defined in "Sparse MLA training backward" (aiter PR #4766), section
+ * "Contract", and in "Tuned sparse MLA prefill for DSv4.1-Flash TP4; fix
+ * attn_sink in Triton fallback" (aiter PR #6002), description items
+ * "attn_sink", "int64 indices" and "Invalid KV rows":
+ *
+ *   for every token t and head h, over the slots j whose row r = idx[t, j]
+ *   lies in [0, num_kv) (any other value is an invalid slot, never read):
+ *     s_j = scale * <q[t,h,:], kv[r,:]>            (K == V == kv, 512 wide)
+ *     m   = max(max_j s_j, sink[h])
+ *     den = sum_j exp(s_j - m) + exp(sink[h] - m)  (sink: denominator only)
+ *     out[t,h,:] = bf16( sum_j exp(s_j - m) * kv[r,:] / den )
+ *     lse[t,h]   = m + ln(den)                     (sink-inclusive, natural log)
+ *   A row with no valid slot gives out = 0 and lse = -inf without a sink
+ *   (or with sink = -inf), lse = sink[h] with a finite sink.
+ *   A duplicated row counts once per slot that names it.
+ *
+ * Ownership: the caller owns every buffer passed in; all pointers except the
+ * stream are device pointers unless stated.  Calls are asynchronous on
+ * `stream` (a cudaStream_t; NULL = the legacy default stream) and return once
+ * the work is queued.  Argument errors are detected on the host before any
+ * CUDA call and leave every buffer untouched.  The library itself allocates
+ * only the split path's partial-result workspace, stream-ordered on `stream`
+ * (cudaMallocAsync / cudaFreeAsync).
+ */
+#ifndef SPARSE_MLA_H
+#define SPARSE_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of topk_indices. */
+typedef enum {
+  SMLA_IDX_INT32 = 0,
+  SMLA_IDX_INT64 = 1
+} smla_index_dtype_t;
+
+/* Return codes.  Every entry point returns one of these. */
+typedef enum {
+  SMLA_OK = 0,
+  SMLA_ERR_NULL_PTR = 1,         /* a required pointer is NULL                      */
+  SMLA_ERR_BAD_SHAPE = 2,        /* T < 0, num_kv < 0 or >= 2^31, topk < 0, ...      */
+  SMLA_ERR_UNSUPPORTED_H = 3,    /* H not in {8, 16, 32, 64, 128}                    */
+  SMLA_ERR_BAD_INDEX_DTYPE = 4,  /* index_dtype not a smla_index_dtype_t value       */
+  SMLA_ERR_MISALIGNED = 5,       /* q, kv or out not 16-byte aligned, lse not 4     */
+  SMLA_ERR_BAD_SCALE = 6,        /* scale is NaN or infinite                         */
+  SMLA_ERR_ALIASING = 7,         /* out or lse overlaps an input                     */
+  SMLA_ERR_CUDA = 8,             /* a CUDA runtime call failed (see _last_cuda_error)*/
+  SMLA_ERR_DEVICE_TIMEOUT = 9,   /* a kernel's bounded wait expired (device status)  */
+  SMLA_ERR_BAD_SPLITS = 10       /* forced split count out of range                  */
+} smla_status_t;
+
+/*
+ * sparse_mla_fwd -- the op.
+ *
+ *   q            [T, H, 512] bf16, contiguous, 16-byte aligned.
+ *   kv           [num_kv, 512] bf16, contiguous, 16-byte aligned; may sit at
+ *                any 16-byte aligned offset inside a larger allocation
+ *                (offsets beyond 2 GiB are fine: all address math is 64-bit).
+ *   topk_indices [T, topk] int32 or int64 (index_dtype), contiguous.  Values
+ *                are compared at their full width: anything outside
+ *                [0, num_kv) is an invalid slot (never an error, never read).
+ *   attn_sink    [H] fp32, or NULL for no sink.  -inf behaves as no sink.
+ *   scale        finite; 1/sqrt(512) for DeepSeek-V4.  Negative is allowed.
+ *   out          [T, H, 512] bf16, contiguous, 16-byte aligned, caller-allocated;
+ *                must not overlap q, kv or topk_indices.
+ *   lse          [T, H] fp32, contiguous, caller-allocated.
+ *   T >= 0 (T == 0: nothing is launched), H in {8,16,32,64,128},
+ *   0 <= num_kv < 2^31, topk >= 0 (num_kv == 0 or topk == 0: every row is
+ *   fully masked).
+ *   stream       cudaStream_t.
+ *
+ * The split count over the topk slots is chosen by the library.
+ */
+smla_status_t sparse_mla_fwd(const void* q, const void* kv, const void* topk_indices,
+                             int32_t index_dtype, const float* attn_sink, float scale,
+                             void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
+                             int32_t topk, void* stream);
+
+/*
+ * sparse_mla_fwd_ex -- sparse_mla_fwd with two test/benchmark controls.
+ *
+ *   num_splits   0 = library choice; otherwise 1..64: the topk slots of each
+ *                token are cut into num_splits contiguous ranges computed
+ *                independently and merged by a combine kernel (the
+ *                split-TOPK path; lse-weighted merge, the sink folded once).
+ *   read_trace   NULL, or a device int64 [T, topk] buffer: the kernel writes,
+ *                for every slot, the kv row it gathers for that slot, or -1
+ *                when the slot is invalid and nothing is read.  Written by
+ *                the same code that forms the gather address.
+ */
+smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_indices,
+                                int32_t index_dtype, const float* attn_sink, float scale,
+                                void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
+                                int32_t topk, void* stream, int32_t num_splits,
+                                int64_t* read_trace);
+
+/*
+ * sparse_mla_plan -- what sparse_mla_fwd_ex would launch, without launching.
+ * Host only (no CUDA call).  Writes the kernel family (0 = small-head kernel,
+ * 1 = tcgen05 H=128 kernel), the split count and the number of kernel
+ * launches per call.  num_splits as in sparse_mla_fwd_ex.
+ */
+smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_splits,
+                              int32_t* kernel_family, int32_t* splits_out,
+                              int32_t* launches_out);
+
+/*
+ * sparse_mla_device_status -- synchronises `stream`, then reads and clears
+ * the library's device error word on the current device.  Returns
+ * SMLA_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait since the last
+ * call (its outputs are then unspecified), SMLA_OK otherwise.
+ */
+smla_status_t sparse_mla_device_status(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* sparse_mla_strerror(int32_t status);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char* sparse_mla_last_cuda_error(void);
+
+/* ABI version: bumped on any incompatible change of the declarations above. */
+int32_t sparse_mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_H */

@@ -1,0 +1,189 @@
+"""Thin Python binding of ``libsparse_mla.so`` (ctypes; argument marshalling only).
+
+The names mirror the C ABI in ``include/sparse_mla.h``.  Torch supplies the
+device memory and the stream; every step of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing
+the calls raise.
+
+Argument checks mirror the pages' public entry ("Tuned sparse MLA prefill for
+DSv4.1-Flash TP4; fix attn_sink in Triton fallback", description: a clear
+error for a q that is not bf16, a kv dtype mismatch and a non-contiguous
+``out``; ``out`` on q's device with a unit-stride last dim; and "Sparse MLA
+training backward", review reply on host tensors: a named device error).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libsparse_mla.so")
+
+SMLA_IDX_INT32 = 0
+SMLA_IDX_INT64 = 1
+SMLA_OK = 0
+
+STATUS = {
+    0: "SMLA_OK", 1: "SMLA_ERR_NULL_PTR", 2: "SMLA_ERR_BAD_SHAPE", 3: "SMLA_ERR_UNSUPPORTED_H",
+    4: "SMLA_ERR_BAD_INDEX_DTYPE", 5: "SMLA_ERR_MISALIGNED", 6: "SMLA_ERR_BAD_SCALE",
+    7: "SMLA_ERR_ALIASING", 8: "SMLA_ERR_CUDA", 9: "SMLA_ERR_DEVICE_TIMEOUT",
+    10: "SMLA_ERR_BAD_SPLITS",
+}
+
+# exported symbol -> (restype, argtypes)
+_P, _I32, _I64, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+_FWD_ARGS = [_P, _P, _P, _I32, _P, _F32, _P, _P, _I64, _I32, _I64, _I32, _P]
+SIGNATURES = {
+    "sparse_mla_fwd": (_I32, _FWD_ARGS),
+    "sparse_mla_fwd_ex": (_I32, _FWD_ARGS + [_I32, _P]),
+    "sparse_mla_plan": (_I32, [_I64, _I32, _I32, _I32, _P, _P, _P]),
+    "sparse_mla_device_status": (_I32, [_P]),
+    "sparse_mla_strerror": (ctypes.c_char_p, [_I32]),
+    "sparse_mla_last_cuda_error": (ctypes.c_char_p, []),
+    "sparse_mla_abi_version": (_I32, []),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class SparseMLAError(RuntimeError):
+    """A non-OK status from the library (``status`` holds the code)."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}: {strerror(status)}"
+        if status == 8:
+            msg += f" [{last_cuda_error()}]"
+        super().__init__(msg)
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library once; raises if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().sparse_mla_strerror(int(status)).decode()
+
+
+def last_cuda_error() -> str:
+    return lib().sparse_mla_last_cuda_error().decode()
+
+
+def abi_version() -> int:
+    return int(lib().sparse_mla_abi_version())
+
+
+def sparse_mla_plan(T: int, H: int, topk: int, num_splits: int = 0):
+    """(kernel_family, splits, launches) the library would use."""
+    fam, sp, ln = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = lib().sparse_mla_plan(T, H, topk, num_splits, ctypes.byref(fam), ctypes.byref(sp),
+                               ctypes.byref(ln))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_plan")
+    return fam.value, sp.value, ln.value
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check_dev(name, x, dev):
+    if not x.is_cuda:
+        raise RuntimeError(f"{name} must be a CUDA tensor, got device {x.device}")
+    if x.device != dev:
+        raise RuntimeError(f"{name} is on {x.device}, expected {dev}")
+
+
+def sparse_mla_fwd(q, kv, topk_indices, attn_sink=None, scale: Optional[float] = None,
+                   out=None, lse=None, num_splits: int = 0, read_trace=None, stream=None):
+    """Sparse MLA prefill forward; returns ``(out, lse)``.
+
+    q ``[T, H, 512]`` bf16; kv ``[num_kv, 512]`` bf16 (K == V); topk_indices
+    ``[T, topk]`` int32/int64 (any value outside ``[0, num_kv)`` is an invalid
+    slot); attn_sink ``[H]`` fp32 or None; scale defaults to 1/sqrt(512).
+    ``out`` (bf16, q's shape) and ``lse`` (fp32 ``[T, H]``) are allocated when
+    not given.  ``num_splits`` and ``read_trace`` are the test controls of
+    ``sparse_mla_fwd_ex``.
+    """
+    import torch
+    if q.dim() != 3 or q.shape[-1] != 512:
+        raise RuntimeError(f"q must be [T, H, 512], got {tuple(q.shape)}")
+    if q.dtype != torch.bfloat16:
+        raise RuntimeError(f"q must be bfloat16, got {q.dtype}")
+    if kv.dtype != q.dtype:
+        raise RuntimeError(f"kv dtype mismatch: kv is {kv.dtype}, q is {q.dtype}")
+    if kv.dim() != 2 or kv.shape[-1] != 512:
+        raise RuntimeError(f"kv must be [num_kv, 512], got {tuple(kv.shape)}")
+    if topk_indices.dtype not in (torch.int32, torch.int64):
+        raise RuntimeError(f"topk_indices must be int32 or int64, got {topk_indices.dtype}")
+    T, H, _ = q.shape
+    if topk_indices.dim() != 2 or topk_indices.shape[0] != T:
+        raise RuntimeError(f"topk_indices must be [T, topk], got {tuple(topk_indices.shape)}")
+    dev = q.device
+    for n, x in (("q", q), ("kv", kv), ("topk_indices", topk_indices)):
+        _check_dev(n, x, dev)
+        if not x.is_contiguous():
+            raise RuntimeError(f"{n} must be contiguous")
+    if attn_sink is not None:
+        _check_dev("attn_sink", attn_sink, dev)
+        if attn_sink.dtype != torch.float32 or tuple(attn_sink.shape) != (H,):
+            raise RuntimeError(f"attn_sink must be float32 [{H}], got {attn_sink.dtype} "
+                               f"{tuple(attn_sink.shape)}")
+        if not attn_sink.is_contiguous():
+            raise RuntimeError("attn_sink must be contiguous")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_dev("out", out, dev)
+        if out.shape != q.shape or out.dtype != q.dtype:
+            raise RuntimeError(f"out must match q ({tuple(q.shape)}, {q.dtype}), got "
+                               f"{tuple(out.shape)}, {out.dtype}")
+        if not out.is_contiguous():
+            raise RuntimeError("out must be contiguous with a unit-stride last dim")
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    else:
+        _check_dev("lse", lse, dev)
+        if tuple(lse.shape) != (T, H) or lse.dtype != torch.float32 or not lse.is_contiguous():
+            raise RuntimeError(f"lse must be contiguous float32 [{T}, {H}]")
+    if read_trace is not None:
+        _check_dev("read_trace", read_trace, dev)
+        if read_trace.dtype != torch.int64 or read_trace.shape != topk_indices.shape:
+            raise RuntimeError("read_trace must be int64 with topk_indices' shape")
+    if scale is None:
+        scale = 512 ** -0.5
+    idt = SMLA_IDX_INT64 if topk_indices.dtype == torch.int64 else SMLA_IDX_INT32
+    with torch.cuda.device(dev):
+        st = lib().sparse_mla_fwd_ex(
+            q.data_ptr(), kv.data_ptr() if kv.numel() else None,
+            topk_indices.data_ptr() if topk_indices.numel() else None, idt,
+            attn_sink.data_ptr() if attn_sink is not None else None, float(scale),
+            out.data_ptr(), lse.data_ptr(), T, H, kv.shape[0], topk_indices.shape[1],
+            _stream_ptr(stream), int(num_splits),
+            read_trace.data_ptr() if read_trace is not None else None)
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_fwd")
+    return out, lse
+
+
+def sparse_mla_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    import torch
+    return int(lib().sparse_mla_device_status(_stream_ptr(stream) if torch.cuda.is_available()
+                                              else None))

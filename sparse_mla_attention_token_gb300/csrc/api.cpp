@@ -1,0 +1,244 @@
+// C ABI of the sparse MLA prefill forward: argument validation, planning
+// (kernel family and split count), launches and status reporting.
+//
+// Validation mirrors the checks of the pages' public entry ("Tuned sparse MLA
+// prefill for DSv4.1-Flash TP4; fix attn_sink in Triton fallback": clear
+// errors for a bad q, a kv mismatch and an unusable out=, out= on q's device
+// with a unit-stride last dim) in C terms: null pointers, shapes, alignment,
+// aliasing and a finite scale, all decided on the host before any CUDA call.
+// Index values are never errors: any value outside [0, num_kv) is an invalid
+// slot, resolved on the device.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "smla_internal.h"
+#include "sparse_mla.h"
+
+namespace {
+
+constexpr int32_t kAbiVersion = 1;
+constexpr int kMaxSplits = 64;
+constexpr int kNumSMs = 152;  // GB300; only used to pick a split count
+
+thread_local char g_last_cuda_error[256] = "";
+
+smla_status_t cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%d)", where,
+                cudaGetErrorString(e), static_cast<int>(e));
+  return SMLA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+struct Plan {
+  int family;    // 0 small-head, 1 tcgen05 H=128
+  int splits;
+  int launches;
+};
+
+smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int32_t num_splits, Plan* pl) {
+  if (num_splits < 0 || num_splits > kMaxSplits) return SMLA_ERR_BAD_SPLITS;
+  const int min_splits =
+      std::max(1, (topk + smla::kSmallHMaxSlots - 1) / smla::kSmallHMaxSlots);
+  int splits;
+  if (num_splits > 0) {
+    splits = num_splits;
+  } else if (H == 128 && smla::h128_supported(T, H, topk)) {
+    splits = 1;
+  } else {
+    // enough CTAs to cover the GPU twice; each split keeps >= 64 slots
+    const int64_t ctas = T * ((H + 15) / 16);
+    splits = 1;
+    if (ctas > 0 && ctas < 2 * kNumSMs) {
+      const int64_t want = (2 * kNumSMs + ctas - 1) / ctas;
+      splits = static_cast<int>(std::min<int64_t>(want, std::max(1, topk / 64)));
+      splits = std::min(splits, 16);
+    }
+  }
+  splits = std::max(splits, min_splits);
+  if (num_splits > 0 && splits != num_splits) return SMLA_ERR_BAD_SPLITS;  // too few for topk
+  if (splits > kMaxSplits) return SMLA_ERR_BAD_SPLITS;
+  const bool tc = (splits == 1) && smla::h128_supported(T, H, topk);
+  pl->family = tc ? 1 : 0;
+  pl->splits = splits;
+  pl->launches = (T == 0) ? 0 : (splits > 1 ? 2 : 1);
+  return SMLA_OK;
+}
+
+smla_status_t validate(const void* q, const void* kv, const void* idx, int32_t index_dtype,
+                       const float* sink, float scale, void* out, float* lse, int64_t T,
+                       int32_t H, int64_t num_kv, int32_t topk, const int64_t* trace) {
+  if (T < 0 || num_kv < 0 || num_kv >= (int64_t(1) << 31) || topk < 0) return SMLA_ERR_BAD_SHAPE;
+  if (T > (int64_t(1) << 31) - 1) return SMLA_ERR_BAD_SHAPE;
+  if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
+  if (index_dtype != SMLA_IDX_INT32 && index_dtype != SMLA_IDX_INT64)
+    return SMLA_ERR_BAD_INDEX_DTYPE;
+  if (!std::isfinite(scale)) return SMLA_ERR_BAD_SCALE;
+  if (T == 0) return SMLA_OK;
+  if (q == nullptr || out == nullptr || lse == nullptr) return SMLA_ERR_NULL_PTR;
+  if (num_kv > 0 && kv == nullptr) return SMLA_ERR_NULL_PTR;
+  if (topk > 0 && idx == nullptr) return SMLA_ERR_NULL_PTR;
+  const uintptr_t isz = index_dtype == SMLA_IDX_INT64 ? 8 : 4;
+  if (!aligned(q, 16) || !aligned(out, 16) || (kv && !aligned(kv, 16)) || !aligned(lse, 4) ||
+      (idx && !aligned(idx, isz)) || (sink && !aligned(sink, 4)) || (trace && !aligned(trace, 8)))
+    return SMLA_ERR_MISALIGNED;
+  const uint64_t qb = uint64_t(T) * H * smla::kHeadDim * 2;
+  const uint64_t kvb = uint64_t(num_kv) * smla::kHeadDim * 2;
+  const uint64_t ib = uint64_t(T) * topk * isz;
+  const uint64_t lb = uint64_t(T) * H * 4;
+  const uint64_t sb = sink ? uint64_t(H) * 4 : 0;
+  const uint64_t tb = trace ? uint64_t(T) * topk * 8 : 0;
+  const void* ins[4] = {q, kv, idx, sink};
+  const uint64_t inb[4] = {qb, kvb, ib, sb};
+  for (int i = 0; i < 4; ++i) {
+    if (overlap(out, qb, ins[i], inb[i]) || overlap(lse, lb, ins[i], inb[i]) ||
+        overlap(trace, tb, ins[i], inb[i]))
+      return SMLA_ERR_ALIASING;
+  }
+  if (overlap(out, qb, lse, lb) || overlap(out, qb, trace, tb) || overlap(lse, lb, trace, tb))
+    return SMLA_ERR_ALIASING;
+  return SMLA_OK;
+}
+
+smla_status_t run(const void* q, const void* kv, const void* idx, int32_t index_dtype,
+                  const float* sink, float scale, void* out, float* lse, int64_t T, int32_t H,
+                  int64_t num_kv, int32_t topk, void* stream, int32_t num_splits,
+                  int64_t* trace) {
+  smla_status_t st =
+      validate(q, kv, idx, index_dtype, sink, scale, out, lse, T, H, num_kv, topk, trace);
+  if (st != SMLA_OK) return st;
+  Plan pl;
+  st = make_plan(T, H, topk, num_splits, &pl);
+  if (st != SMLA_OK) return st;
+  if (T == 0) return SMLA_OK;
+
+  smla::FwdParams p{};
+  p.q = q;
+  p.kv = kv;
+  p.idx = idx;
+  p.sink = sink;
+  p.out = out;
+  p.lse = lse;
+  p.trace = trace;
+  p.T = T;
+  p.num_kv = num_kv;
+  p.H = H;
+  p.topk = topk;
+  p.splits = pl.splits;
+  p.idx64 = index_dtype == SMLA_IDX_INT64 ? 1 : 0;
+  p.scale = scale;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (pl.family == 1) {
+    const int e = smla::launch_h128(p, stream);
+    if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "h128 kernel launch");
+    return SMLA_OK;
+  }
+  if (pl.splits == 1) {
+    const int e = smla::launch_smallh(p, stream);
+    if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "small-head kernel launch");
+    return SMLA_OK;
+  }
+  // split path: stream-ordered workspace for the partials
+  const uint64_t rows = uint64_t(pl.splits) * uint64_t(T) * uint64_t(H);
+  const size_t bytes = rows * smla::kHeadDim * 4 + rows * 4;
+  void* ws = nullptr;
+  cudaError_t ce = cudaMallocAsync(&ws, bytes, s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaMallocAsync(split workspace)");
+  p.part_o = static_cast<float*>(ws);
+  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + rows * smla::kHeadDim * 4);
+  int e = smla::launch_smallh(p, stream);
+  if (e == 0) e = smla::launch_combine(p, stream);
+  ce = cudaFreeAsync(ws, s);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "split path launch");
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaFreeAsync(split workspace)");
+  return SMLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+smla_status_t sparse_mla_fwd(const void* q, const void* kv, const void* topk_indices,
+                             int32_t index_dtype, const float* attn_sink, float scale,
+                             void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
+                             int32_t topk, void* stream) {
+  return run(q, kv, topk_indices, index_dtype, attn_sink, scale, out, lse, T, H, num_kv, topk,
+             stream, 0, nullptr);
+}
+
+smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_indices,
+                                int32_t index_dtype, const float* attn_sink, float scale,
+                                void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
+                                int32_t topk, void* stream, int32_t num_splits,
+                                int64_t* read_trace) {
+  return run(q, kv, topk_indices, index_dtype, attn_sink, scale, out, lse, T, H, num_kv, topk,
+             stream, num_splits, read_trace);
+}
+
+smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_splits,
+                              int32_t* kernel_family, int32_t* splits_out,
+                              int32_t* launches_out) {
+  if (T < 0 || topk < 0) return SMLA_ERR_BAD_SHAPE;
+  if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
+  Plan pl;
+  const smla_status_t st = make_plan(T, H, topk, num_splits, &pl);
+  if (st != SMLA_OK) return st;
+  if (kernel_family) *kernel_family = pl.family;
+  if (splits_out) *splits_out = pl.splits;
+  if (launches_out) *launches_out = pl.launches;
+  return SMLA_OK;
+}
+
+smla_status_t sparse_mla_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int* word = nullptr;
+  const int ge = smla::h128_error_word(&word);
+  if (ge != 0) return cuda_fail(static_cast<cudaError_t>(ge), "cudaGetSymbolAddress(error word)");
+  if (word == nullptr) return SMLA_OK;
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    return SMLA_ERR_DEVICE_TIMEOUT;
+  }
+  return SMLA_OK;
+}
+
+const char* sparse_mla_strerror(int32_t status) {
+  switch (status) {
+    case SMLA_OK: return "ok";
+    case SMLA_ERR_NULL_PTR: return "a required pointer is NULL";
+    case SMLA_ERR_BAD_SHAPE: return "bad shape (T, num_kv or topk out of range)";
+    case SMLA_ERR_UNSUPPORTED_H: return "unsupported head count (H must be 8, 16, 32, 64 or 128)";
+    case SMLA_ERR_BAD_INDEX_DTYPE: return "index dtype must be int32 or int64";
+    case SMLA_ERR_MISALIGNED: return "misaligned buffer (q, kv, out need 16 bytes)";
+    case SMLA_ERR_BAD_SCALE: return "scale must be finite";
+    case SMLA_ERR_ALIASING: return "an output buffer overlaps another buffer";
+    case SMLA_ERR_CUDA: return "CUDA runtime error";
+    case SMLA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (outputs unspecified)";
+    case SMLA_ERR_BAD_SPLITS: return "split count out of range for this topk";
+    default: return "unknown status";
+  }
+}
+
+const char* sparse_mla_last_cuda_error(void) { return g_last_cuda_error; }
+
+int32_t sparse_mla_abi_version(void) { return kAbiVersion; }
+
+}  // extern "C"

@@ -1,0 +1,329 @@
+// Small-head sparse MLA prefill forward (H = 8/16 per rank, head groups of 16).
+//
+// One CTA computes one (token, group of 16 heads, slot range).  The op
+// ("Sparse MLA training backward", section "Contract"; the forward's
+// has_pe=False path) is gather-bound at these head counts: every gathered
+// 1 KB kv row feeds only H <= 16 query rows ("Tuned sparse MLA prefill for
+// DSv4.1-Flash TP4", description "Perf": the 32-row head tile of the
+// autotuned launch is half masked at 16 heads).  So the design spends its
+// effort on the gather:
+//
+//   * the token's index list is classified on the index's full width
+//     (0 <= idx < num_kv; int64 never narrowed before the check) and the valid
+//     rows are compacted, in slot order, into a shared-memory row list;
+//     invalid slots are never read (PR #6002 "Invalid KV rows");
+//   * rows are gathered 64 per tile with 16-byte cp.async into a two-stage
+//     ring (the next tile lands while this one is computed); the ragged tail
+//     of the last tile is zero-filled, so no pad row can inject NaN;
+//   * M = 16 heads is below tcgen05's smallest tile (M = 64), so the two
+//     contractions use warp-level mma.sync m16n8k16 (bf16 in, fp32 out):
+//     the 8 warps split the 512-wide head dim, each owning 64 columns of
+//     both S = Q.K^T (partial over its columns, summed across warps in
+//     shared memory) and O += P.V;
+//   * online softmax in base 2 (exp2 of scale*log2e-scaled scores), the sink
+//     folded once in the epilogue: m' = max(m, sink), l' = l 2^(m-m') +
+//     2^(sink-m'), lse = ln2 (m' + log2 l') (PR #4766 "Contract" and the
+//     sink-inclusive lse note).
+//
+// Split mode (splits > 1): each slot range writes its sink-free partial
+// (O normalised by its own sum, lse of its own slots) for the combine kernel.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "smla_device.cuh"
+#include "smla_internal.h"
+
+namespace smla {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kBN = 64;           // gathered rows per tile
+constexpr int kHG = 16;           // heads per CTA (mma M)
+constexpr int kSredStride = 72;   // floats per row of a warp's partial scores (bank spread)
+constexpr int kPStride = 72;      // bf16 per row of P (bank spread for ldmatrix)
+constexpr int kOStride = 520;     // bf16 per row of the staged output tile (bank spread)
+constexpr int kRowBytes = kHeadDim * 2;
+
+struct __align__(128) Smem {
+  __nv_bfloat16 kv[2][kBN * kHeadDim];     // 2 x 64 KB; 16 B chunk c of row r at c ^ (r & 7)
+  float sred[kWarps][kHG * kSredStride];   // per-warp partial scores
+  __nv_bfloat16 p[kHG * kPStride];         // probabilities, A operand of P.V
+  float alpha[kHG];                        // per-row rescale of O for the current tile
+  float row_m[kHG];                        // final running max (log2 units)
+  float row_l[kHG];                        // final running sum
+  int rows[kSmallHMaxSlots];               // compacted valid kv rows, slot order
+  int warp_cnt[kWarps];
+};
+
+__device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t base, int r, int c) {
+  return base + r * kRowBytes + ((c ^ (r & 7)) << 4);
+}
+
+template <typename IdxT, bool kSplit>
+__global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int g = lane >> 2;    // mma groupID
+  const int tig = lane & 3;   // mma thread-in-group
+  const int64_t t = blockIdx.x;
+  const int hg = blockIdx.y;
+  const int split = blockIdx.z;
+  const int H = p.H;
+  const int h0 = hg * kHG;
+  const int hvalid = min(kHG, H - h0);
+
+  const int chunk = (p.topk + p.splits - 1) / p.splits;
+  const int j0 = min(p.topk, split * chunk);
+  const int j1 = min(p.topk, j0 + chunk);
+  const IdxT* idx = static_cast<const IdxT*>(p.idx) + t * p.topk;
+
+  // ---- 1. classify every slot at full width, compact the valid rows (slot order)
+  int nvalid = 0;
+  for (int base = j0; base < j1; base += kThreads) {
+    const int j = base + tid;
+    bool v = false;
+    int row = -1;
+    if (j < j1) {
+      const IdxT x = idx[j];
+      v = slot_valid<IdxT>(x, p.num_kv);
+      if (v) row = static_cast<int>(x);   // exact: num_kv < 2^31
+      if (p.trace != nullptr && hg == 0) p.trace[t * p.topk + j] = v ? row : -1;
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) sm.warp_cnt[warp] = __popc(ball);
+    __syncthreads();
+    int off = nvalid, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = sm.warp_cnt[w];
+      off += (w < warp) ? c : 0;
+      total += c;
+    }
+    if (v) sm.rows[off + __popc(ball & ((1u << lane) - 1u))] = row;
+    nvalid += total;
+    __syncthreads();
+  }
+
+  // ---- 2. this warp's Q fragments: rows = heads of the group, k = its 64 columns
+  uint32_t qa[4][4];
+  {
+    const uint32_t* q32 = static_cast<const uint32_t*>(p.q);
+    const int64_t rbase = (t * H + h0) * kHeadDim;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int d = warp * 64 + kk * 16 + 2 * tig;
+      const bool lo = g < hvalid, hi = (g + 8) < hvalid;
+      qa[kk][0] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d) >> 1] : 0u;
+      qa[kk][1] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d) >> 1] : 0u;
+      qa[kk][2] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d + 8) >> 1] : 0u;
+      qa[kk][3] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d + 8) >> 1] : 0u;
+    }
+  }
+
+  const char* kvb = static_cast<const char*>(p.kv);
+  auto issue_tile = [&](int tile, int stage) {
+    const uint32_t dst0 = smem_u32(sm.kv[stage]);
+#pragma unroll 4
+    for (int i = tid; i < kBN * 64; i += kThreads) {
+      const int r = i >> 6, c = i & 63;
+      const int slot = tile * kBN + r;
+      const bool ok = slot < nvalid;
+      const char* src = ok ? kvb + int64_t(sm.rows[slot]) * kRowBytes + c * 16 : kvb;
+      cp_async_16(kv_chunk_addr(dst0, r, c), src, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+
+  const int ntiles = (nvalid + kBN - 1) / kBN;
+  const float sl2 = p.scale * kLog2e;
+  const int srow = 2 * warp + (lane >> 4);   // softmax row owned by this half-warp
+  const int sc0 = (lane & 15) * 4;           // its 4 columns
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  if (ntiles > 0) issue_tile(0, 0);
+  for (int it = 0; it < ntiles; ++it) {
+    const int stage = it & 1;
+    cp_async_wait<0>();
+    __syncthreads();  // tile `it` landed; every warp is done with the other stage
+    if (it + 1 < ntiles) issue_tile(it + 1, stage ^ 1);
+    const uint32_t kvs = smem_u32(sm.kv[stage]);
+
+    // ---- 3. partial S over this warp's 64 columns
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int kp = 0; kp < 2; ++kp) {
+      const int c = warp * 8 + kp * 4 + (lane >> 3);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int r = nt * 8 + (lane & 7);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(kv_chunk_addr(kvs, r, c), b0, b1, b2, b3);
+        mma_16816(s[nt], qa[2 * kp], b0, b1);
+        mma_16816(s[nt], qa[2 * kp + 1], b2, b3);
+      }
+    }
+    float* sw = sm.sred[warp];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      *reinterpret_cast<float2*>(&sw[g * kSredStride + nt * 8 + 2 * tig]) =
+          make_float2(s[nt][0], s[nt][1]);
+      *reinterpret_cast<float2*>(&sw[(g + 8) * kSredStride + nt * 8 + 2 * tig]) =
+          make_float2(s[nt][2], s[nt][3]);
+    }
+    __syncthreads();
+
+    // ---- 4. reduce the 8 partials, online softmax (base 2)
+    {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(&sm.sred[w][srow * kSredStride + sc0]);
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+      }
+      const int col = it * kBN + sc0;
+      float x0 = (col + 0 < nvalid) ? a.x * sl2 : -INFINITY;
+      float x1 = (col + 1 < nvalid) ? a.y * sl2 : -INFINITY;
+      float x2 = (col + 2 < nvalid) ? a.z * sl2 : -INFINITY;
+      float x3 = (col + 3 < nvalid) ? a.w * sl2 : -INFINITY;
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m_run, mx);  // finite: the tile holds >= 1 valid row
+      const float alpha = ex2(m_run - m_new);
+      const float e0 = ex2(x0 - m_new), e1 = ex2(x1 - m_new);
+      const float e2 = ex2(x2 - m_new), e3 = ex2(x3 - m_new);
+      float ps = (e0 + e1) + (e2 + e3);
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l_run = l_run * alpha + ps;
+      m_run = m_new;
+      uint2 pk;
+      pk.x = pack_bf16x2(e0, e1);
+      pk.y = pack_bf16x2(e2, e3);
+      *reinterpret_cast<uint2*>(&sm.p[srow * kPStride + sc0]) = pk;
+      if ((lane & 15) == 0) sm.alpha[srow] = alpha;
+    }
+    __syncthreads();
+
+    // ---- 5. O = alpha * O + P . V over this warp's 64 columns
+    {
+      const float a_lo = sm.alpha[g], a_hi = sm.alpha[g + 8];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        acc[nt][0] *= a_lo; acc[nt][1] *= a_lo;
+        acc[nt][2] *= a_hi; acc[nt][3] *= a_hi;
+      }
+      const uint32_t ps = smem_u32(sm.p);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t pa[4];
+        const int pr = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int pc = ks * 16 + (lane >> 4) * 8;
+        ldmatrix_x4(ps + (pr * kPStride + pc) * 2, pa[0], pa[1], pa[2], pa[3]);
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          const int j = lane >> 3;
+          const int r = ks * 16 + (j & 1) * 8 + (lane & 7);
+          const int c = warp * 8 + np * 2 + (j >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(kv_chunk_addr(kvs, r, c), b0, b1, b2, b3);
+          mma_16816(acc[2 * np], pa, b0, b1);
+          mma_16816(acc[2 * np + 1], pa, b2, b3);
+        }
+      }
+    }
+  }
+
+  // ---- 6. epilogue
+  if ((lane & 15) == 0) {
+    sm.row_m[srow] = m_run;
+    sm.row_l[srow] = l_run;
+  }
+  __syncthreads();
+
+  if constexpr (kSplit) {
+    // sink-free partial: O normalised by its own sum; lse of this range alone
+    const int64_t TH = p.T * H;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int r = g + half * 8;
+      if (r >= hvalid) continue;
+      const float m = sm.row_m[r], l = sm.row_l[r];
+      const float f = (l > 0.f) ? 1.f / l : 0.f;
+      const int64_t rowid = int64_t(split) * TH + t * H + h0 + r;
+      float* po = p.part_o + rowid * kHeadDim + warp * 64 + 2 * tig;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+        *reinterpret_cast<float2*>(po + nt * 8) =
+            make_float2(acc[nt][2 * half] * f, acc[nt][2 * half + 1] * f);
+      if (warp == 0 && tig == 0) p.part_lse[rowid] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+  } else {
+    // fold the sink once, normalise, round to bf16, stage, store 16 B per thread
+    __nv_bfloat16* ost = sm.kv[0];   // all warps finished reading the kv ring above
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int r = g + half * 8;
+      const float m = sm.row_m[r], l = sm.row_l[r];
+      float m2 = m, l2 = l;
+      if (p.sink != nullptr && r < hvalid) {
+        const float sk = p.sink[h0 + r] * kLog2e;
+        m2 = fmaxf(m, sk);
+        if (m2 != -INFINITY) l2 = l * ex2(m - m2) + ex2(sk - m2);
+      }
+      const bool live = (m2 != -INFINITY) && (l2 > 0.f);
+      const float f = live ? ex2(m - m2) / l2 : 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+        *reinterpret_cast<uint32_t*>(&ost[r * kOStride + warp * 64 + nt * 8 + 2 * tig]) =
+            pack_bf16x2(acc[nt][2 * half] * f, acc[nt][2 * half + 1] * f);
+      if (warp == 0 && tig == 0 && r < hvalid)
+        p.lse[t * H + h0 + r] = live ? (m2 + log2f(l2)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    uint4* outp = reinterpret_cast<uint4*>(static_cast<char*>(p.out) +
+                                           (t * H + h0) * int64_t(kRowBytes));
+    for (int i = tid; i < hvalid * 64; i += kThreads) {
+      const int r = i >> 6, c = i & 63;
+      outp[i] = *reinterpret_cast<const uint4*>(&ost[r * kOStride + c * 8]);
+    }
+  }
+}
+
+template <typename IdxT, bool kSplit>
+cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
+  auto kern = smallh_fwd_kernel<IdxT, kSplit>;
+  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>((p.H + kHG - 1) / kHG),
+                  static_cast<unsigned>(p.splits));
+  kern<<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_smallh(const FwdParams& p, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool split = p.splits > 1;
+  cudaError_t e;
+  if (p.idx64)
+    e = split ? launch_typed<int64_t, true>(p, s) : launch_typed<int64_t, false>(p, s);
+  else
+    e = split ? launch_typed<int32_t, true>(p, s) : launch_typed<int32_t, false>(p, s);
+  return static_cast<int>(e);
+}
+
+}  // namespace smla

@@ -1,0 +1,244 @@
+"""GPU parity of the CUDA path against the fp64 oracle (needs a GB300).
+
+Every call goes through the C ABI (``sparse_mla_fwd_ex`` via the ctypes
+binding).  Small workloads are compared in full; full-size workloads run at
+their real size, in the launch configuration the benchmark uses, and are
+compared on sampled tokens the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+from sparse_mla_attention_token_gb300 import synth
+from tests.parity import compare, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_mla_attention_token_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _sample_tokens(T, n=256, seed=0):
+    rng = np.random.default_rng(seed)
+    head = np.arange(min(T, 48))
+    tail = np.arange(max(0, T - 48), T)
+    mid = rng.choice(T, size=min(T, n), replace=False)
+    return np.unique(np.concatenate([head, tail, mid]))
+
+
+def _run(B, x, splits=0, trace=False, **dev_kw):
+    q, kv, idx, sink, keep = to_dev(x, DEV, **dev_kw)
+    tr = torch.full(idx.shape, -7, dtype=torch.int64, device=DEV) if trace else None
+    out, lse = B.sparse_mla_fwd(q, kv, idx, sink, x["scale"], num_splits=splits, read_trace=tr)
+    torch.cuda.synchronize()
+    assert B.sparse_mla_device_status() == 0
+    return out, lse, tr
+
+
+# ------------------------------------------------------------ the workloads
+@pytest.mark.parametrize("name", ["tiny", "sweep_k32", "sweep_k128", "sweep_k256", "sweep_k640",
+                                  "sweep_k640_nosink"])
+def test_config_full(B, name):
+    cfg = synth.CONFIGS[name]
+    x = synth.make_inputs(cfg)
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+@pytest.mark.parametrize("name", ["small_head", "h128", "h128_long"])
+def test_config_full_size_sampled(B, name):
+    cfg = synth.CONFIGS[name]
+    x = synth.make_inputs(cfg)
+    kw = {}
+    if cfg.kv_offset_bytes:
+        # kv > 2 GiB into one allocation, NaN guard rows right after num_kv
+        kw = dict(kv_offset_bytes=cfg.kv_offset_bytes, guard_rows=8, guard_value=0x7FC0)
+    out, lse, _ = _run(B, x, **kw)
+    toks = _sample_tokens(cfg.T)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"], tokens=toks)
+    compare(out, lse, O, L, tokens=toks)
+
+
+# ------------------------------------------------------------ index handling
+def _tiny_x(seed=0, sink=True, **cfg_kw):
+    cfg = synth.CONFIGS["tiny"].with_(seed=seed, sink=sink, **cfg_kw)
+    return cfg, synth.make_inputs(cfg)
+
+
+@pytest.mark.parametrize("variant", ["shuffled", "dups", "oob32", "oob64", "nosink", "sinkneg"])
+def test_tiny_variants(B, variant):
+    cfg, x = _tiny_x(seed=31, sink=(variant != "nosink"))
+    if variant == "shuffled":
+        x["idx"] = synth.shuffle_rows(x["idx"], 1)
+    elif variant == "dups":
+        x["idx"] = synth.inject_duplicates(x["idx"], cfg.num_kv, 2, frac=0.25)
+    elif variant == "oob32":
+        x["idx"] = synth.inject_out_of_range(x["idx"], cfg.num_kv, 3, frac=0.3)
+    elif variant == "oob64":
+        x["idx"] = synth.inject_out_of_range(x["idx"].astype(np.int64), cfg.num_kv, 4, frac=0.3)
+    elif variant == "sinkneg":
+        x["sink"] = np.full_like(x["sink"], -np.inf)
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+@pytest.mark.parametrize("dtype", [np.int32, np.int64])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_read_trace_bit_exact(B, dtype, splits):
+    cfg, x = _tiny_x(seed=5)
+    x["idx"] = synth.inject_out_of_range(x["idx"].astype(dtype), cfg.num_kv, 9, frac=0.35)
+    out, lse, tr = _run(B, x, splits=splits, trace=True)
+    want = np.where(orc.valid_slots(x["idx"], cfg.num_kv), x["idx"].astype(np.int64), -1)
+    np.testing.assert_array_equal(tr.cpu().numpy(), want)
+
+
+def test_poisoned_rows_and_guard_never_read(B):
+    cfg, x = _tiny_x(seed=6)
+    idx = x["idx"].copy()
+    idx[idx == 0] = -1
+    used = np.unique(idx[(idx >= 0) & (idx < cfg.num_kv)])
+    poison = np.setdiff1d(np.arange(cfg.num_kv), used)
+    assert 0 in poison and len(poison) >= 1
+    kv_p = x["kv"].copy()
+    kv_p[poison] = 0x7FC0                  # NaN rows no valid slot names
+    x2 = dict(x, idx=synth.inject_out_of_range(idx, cfg.num_kv, 10, frac=0.2), kv=kv_p)
+    out, lse, _ = _run(B, x2, guard_rows=16, guard_value=0x7FC0)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x2["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+@pytest.mark.parametrize("sink", [True, False])
+def test_all_invalid_rows(B, sink):
+    cfg, x = _tiny_x(seed=7, sink=sink)
+    x["idx"] = np.full_like(x["idx"], -1)
+    x["idx"][::3, 5] = cfg.num_kv
+    x["idx"][1::4, 0] = 2 ** 31 - 1
+    out, lse, _ = _run(B, x)
+    assert torch.all(out == 0)
+    L = lse.cpu().numpy()
+    if sink:
+        np.testing.assert_allclose(L, np.broadcast_to(x["sink"], L.shape), rtol=0, atol=2e-6)
+    else:
+        assert np.all(np.isneginf(L))
+
+
+def test_mixed_empty_and_full_rows(B):
+    cfg, x = _tiny_x(seed=8)
+    x["idx"][::2] = -1                      # every other token fully masked
+    for splits in (0, 1, 4):
+        out, lse, _ = _run(B, x, splits=splits)
+        O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+        compare(out, lse, O, L)
+
+
+# ------------------------------------------------------------ split-TOPK path
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 7, 16])
+def test_forced_splits_match_oracle(B, splits):
+    cfg = synth.CONFIGS["sweep_k640"].with_(T=256)
+    x = synth.make_inputs(cfg)
+    out, lse, _ = _run(B, x, splits=splits)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+def test_split_vs_unsplit(B):
+    cfg = synth.CONFIGS["small_head"].with_(T=512)
+    x = synth.make_inputs(cfg)
+    o1, l1, _ = _run(B, x, splits=1)
+    o4, l4, _ = _run(B, x, splits=4)
+    d = (o1.float() - o4.float()).abs().max().item()
+    assert d <= 2e-2
+    fin = torch.isfinite(l1)
+    assert torch.equal(fin, torch.isfinite(l4))
+    assert (l1[fin] - l4[fin]).abs().max().item() <= 5e-3
+
+
+# ------------------------------------------------------------ shapes and edges
+@pytest.mark.parametrize("H", [8, 16, 32, 64, 128])
+def test_head_counts(B, H):
+    cfg = synth.CONFIGS["tiny"].with_(H=H, T=96, pool=24, seed=12)
+    x = synth.make_inputs(cfg)
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+@pytest.mark.parametrize("topk,window", [(1, 1), (3, 2), (67, 40), (130, 64), (2500, 200)])
+def test_ragged_topk(B, topk, window):
+    cfg = synth.CONFIGS["tiny"].with_(T=150, pool=600, ratio=1, topk=topk, window=window, seed=13)
+    x = synth.make_inputs(cfg)
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+def test_topk_zero_and_empty_pool(B):
+    cfg, x = _tiny_x(seed=14)
+    x0 = dict(x, idx=np.zeros((cfg.T, 0), dtype=np.int32))
+    out, lse, _ = _run(B, x0)
+    assert torch.all(out == 0)
+    np.testing.assert_allclose(lse.cpu().numpy(), np.broadcast_to(x["sink"], (cfg.T, cfg.H)),
+                               atol=2e-6)
+    # empty pool: num_kv = 0, every slot invalid
+    xe = dict(x, kv=np.zeros((0, 512), dtype=np.uint16))
+    out, lse, _ = _run(B, xe)
+    assert torch.all(out == 0)
+
+
+def test_single_token(B):
+    cfg, x = _tiny_x(seed=15)
+    x1 = dict(x, q=x["q"][40:41], idx=x["idx"][40:41])
+    out, lse, _ = _run(B, x1)
+    O, L = orc.sparse_mla_fwd(x1["q"], x1["kv"], x1["idx"], x1["sink"], x1["scale"])
+    compare(out, lse, O, L)
+
+
+def test_out_buffer_bit_identical_to_allocating_call(B):
+    cfg, x = _tiny_x(seed=16)
+    q, kv, idx, sink, _ = to_dev(x, DEV)
+    o1, l1 = B.sparse_mla_fwd(q, kv, idx, sink, x["scale"])
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((cfg.T, cfg.H), float("nan"), device=DEV)
+    o2, l2 = B.sparse_mla_fwd(q, kv, idx, sink, x["scale"], out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert o2.data_ptr() == out.data_ptr() and l2.data_ptr() == lse.data_ptr()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_binding_rejections(B):
+    cfg, x = _tiny_x(seed=17)
+    q, kv, idx, sink, _ = to_dev(x, DEV)
+    with pytest.raises(RuntimeError, match="kv dtype mismatch"):
+        B.sparse_mla_fwd(q, kv.to(torch.float16), idx, sink)
+    with pytest.raises(RuntimeError, match="bfloat16"):
+        B.sparse_mla_fwd(q.float(), kv, idx, sink)
+    with pytest.raises(RuntimeError, match="CUDA tensor"):
+        B.sparse_mla_fwd(q, kv.cpu(), idx, sink)
+    with pytest.raises(RuntimeError, match="contiguous"):
+        out = torch.empty(cfg.T, cfg.H, 1024, dtype=torch.bfloat16, device=DEV)[..., ::2]
+        B.sparse_mla_fwd(q, kv, idx, sink, out=out)
+    with pytest.raises(RuntimeError, match="int32 or int64"):
+        B.sparse_mla_fwd(q, kv, idx.to(torch.int16), sink)
+    with pytest.raises(B.SparseMLAError):
+        B.sparse_mla_fwd(q, kv, idx, sink, scale=float("nan"))
+
+
+def test_deterministic(B):
+    cfg = synth.CONFIGS["sweep_k256"].with_(T=512)
+    x = synth.make_inputs(cfg)
+    a, la, _ = _run(B, x)
+    b, lb, _ = _run(B, x)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(la.view(torch.int32), lb.view(torch.int32))
