@@ -47,14 +47,15 @@ struct Plan {
   int launches;
 };
 
-smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int32_t num_splits, Plan* pl) {
+smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int64_t num_kv, int32_t num_splits,
+                        Plan* pl) {
   if (num_splits < 0 || num_splits > kMaxSplits) return SMLA_ERR_BAD_SPLITS;
   const int min_splits =
       std::max(1, (topk + smla::kSmallHMaxSlots - 1) / smla::kSmallHMaxSlots);
   int splits;
   if (num_splits > 0) {
     splits = num_splits;
-  } else if (H == 128 && smla::h128_supported(T, H, topk)) {
+  } else if (smla::h128_supported(T, H, topk, num_kv)) {
     splits = 1;
   } else {
     // enough CTAs to cover the GPU twice; each split keeps >= 64 slots
@@ -69,7 +70,7 @@ smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int32_t num_splits, 
   splits = std::max(splits, min_splits);
   if (num_splits > 0 && splits != num_splits) return SMLA_ERR_BAD_SPLITS;  // too few for topk
   if (splits > kMaxSplits) return SMLA_ERR_BAD_SPLITS;
-  const bool tc = (splits == 1) && smla::h128_supported(T, H, topk);
+  const bool tc = (splits == 1) && smla::h128_supported(T, H, topk, num_kv);
   pl->family = tc ? 1 : 0;
   pl->splits = splits;
   pl->launches = (T == 0) ? 0 : (splits > 1 ? 2 : 1);
@@ -119,7 +120,7 @@ smla_status_t run(const void* q, const void* kv, const void* idx, int32_t index_
       validate(q, kv, idx, index_dtype, sink, scale, out, lse, T, H, num_kv, topk, trace);
   if (st != SMLA_OK) return st;
   Plan pl;
-  st = make_plan(T, H, topk, num_splits, &pl);
+  st = make_plan(T, H, topk, num_kv, num_splits, &pl);
   if (st != SMLA_OK) return st;
   if (T == 0) return SMLA_OK;
 
@@ -193,7 +194,7 @@ smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_sp
   if (T < 0 || topk < 0) return SMLA_ERR_BAD_SHAPE;
   if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
   Plan pl;
-  const smla_status_t st = make_plan(T, H, topk, num_splits, &pl);
+  const smla_status_t st = make_plan(T, H, topk, 1, num_splits, &pl);
   if (st != SMLA_OK) return st;
   if (kernel_family) *kernel_family = pl.family;
   if (splits_out) *splits_out = pl.splits;

@@ -1,18 +1,649 @@
-// tcgen05 kernel for H = 128 (not yet enabled: the planner routes H = 128 to
-// the small-head kernel until this kernel passes parity).
+// tcgen05 sparse MLA prefill forward for H = 128 (one token per 2-CTA cluster).
+//
+// The op is the has_pe=False forward of "Sparse MLA training backward"
+// (aiter PR #4766, section "Contract"): all 128 heads of a token share the
+// token's gathered kv rows, so heads are the MMA M dimension (M = 128).
+//
+// Why a CTA pair.  O[128 x 512] in fp32 is 256 KB, the whole tensor memory
+// of one SM, and S needs a 512-deep contraction.  Each CTA of the pair owns
+// one 256-wide half of the head dim (rank r: columns 256r..256r+255):
+//   * S_r = Q[:, half r] . K[:, half r]^T (partial over its half), the two
+//     partials exchanged through distributed shared memory (fp32) and summed
+//     as own + peer, which is bit-identical in both CTAs;
+//   * both CTAs run the same online softmax on the same S;
+//   * O[:, half r] += P . V[:, half r] into its own TMEM.
+//   TMEM per CTA: O half 256 columns + two 64-column S buffers.
+//
+// Data movement.  The producer warp compacts the token's valid slots
+// (0 <= idx < num_kv at the index's full width; PR #6002 "Invalid KV rows",
+// "int64 indices") into a row list, loads the token's Q half with 2-D TMA and
+// gathers 64 rows per tile with TMA gather4 (half rows, 512 B each) into a
+// 3-stage ring in the 128-byte-swizzled layout.  One tile serves as the
+// K-major B operand of Q.K^T and the MN-major B operand of P.V.  The ragged
+// tail of the last tile repeats a valid row (its scores are masked to -inf,
+// its probability is exactly 0), so no invalid slot is ever read.
+//
+// Warp roles (192 threads): warp 0 producer, warp 1 TMEM owner and
+// single-thread MMA issuer, warps 2..5 softmax + epilogue (thread = TMEM lane =
+// head).  Softmax is base 2 with the sink folded once in the epilogue
+// (m' = max(m, sink), l' = l 2^(m-m') + 2^(sink-m'), lse = ln2 (m' + log2 l'));
+// the running max is only raised when it grows by more than 2^8, which keeps
+// O rescales rare and is exact because O and l use the same stale max.
+//
+// Every mbarrier wait is bounded: on expiry the kernel sets an error word,
+// every role leaves its loop, in-flight copies and MMAs are drained with
+// bounded waits, TMEM is freed and the kernel returns.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
+#include <cmath>
+#include <mutex>
+
+#include "smla_device.cuh"
 #include "smla_internal.h"
+#include "smla_sm100.cuh"
 
 namespace smla {
+namespace {
 
-bool h128_supported(int64_t, int32_t, int32_t) { return false; }
+using namespace sm100;
 
-int launch_h128(const FwdParams&, void*) { return static_cast<int>(cudaErrorNotSupported); }
+constexpr int kThreads = 192;
+constexpr int kTileN = 64;            // slots per tile
+constexpr int kStages = 3;
+constexpr int kMaxTopk = 2048;        // row-list capacity
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 256;      // S buffers start at this column (O at 0)
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr uint32_t kQOff = 0;                         // [4 col blocks][128 rows][128 B]
+constexpr uint32_t kQBytes = 128 * 256 * 2;           // 64 KB
+constexpr uint32_t kKVOff = kQOff + kQBytes;          // [stage][4 col blocks][64 rows][128 B]
+constexpr uint32_t kStageBytes = kTileN * 256 * 2;    // 32 KB
+constexpr uint32_t kPOff = kKVOff + kStages * kStageBytes;   // [128 rows][128 B] bf16
+constexpr uint32_t kPBytes = 128 * kTileN * 2;        // 16 KB
+constexpr uint32_t kXOff = kPOff + kPBytes;           // peer's partial S: [128 rows][64 fp32]
+constexpr uint32_t kXBytes = 128 * kTileN * 4;        // 32 KB
+constexpr uint32_t kRowsOff = kXOff + kXBytes;        // int32 row list
+constexpr uint32_t kBarOff = kRowsOff + kMaxTopk * 4;
+constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024; // + barriers + alignment slack
+
+constexpr long long kTimeoutCycles = 4000000000LL;    // ~2 s at 2 GHz
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done;
+  uint64_t x_full, x_free;
+  uint64_t o_free;
+  uint64_t meta_full[2], meta_empty[2];
+  uint64_t drain;
+  int nvalid[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct H128Params {
+  const void* idx;
+  const float* sink;
+  __nv_bfloat16* out;
+  float* lse;
+  int64_t* trace;
+  unsigned int* err;
+  int64_t T;
+  int64_t num_kv;
+  int32_t topk;
+  int32_t idx64;
+  float scale;
+};
+
+__device__ unsigned int g_h128_error;
+
+// Bounded mbarrier wait; false on timeout or (unless kDrain) when another role
+// gave up.  Drain waits ignore the abort flag: they wait for work already in
+// flight (copies, MMAs), bounded by time alone.
+template <bool kClusterScope, bool kDrain = false>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Bars* b, unsigned* err,
+                                         unsigned code) {
+  if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+      return true;
+    if ((n & 15) == 0) {
+      if (!kDrain && *reinterpret_cast<volatile int*>(&b->abort_flag)) return false;
+      if (clock64() - t0 > kTimeoutCycles) {
+        *reinterpret_cast<volatile int*>(&b->abort_flag) = 1;
+        atomicOr(err, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t& b) { return smem_u32(&b); }
+
+// Compact one token's valid slots (slot order) into `rows`; returns the count.
+// Warp-collective (warp 0).  Loads are issued kUnroll deep before use.
+template <typename IdxT>
+__device__ __forceinline__ int compact_token(const H128Params& p, int64_t tok, int* rows,
+                                             bool write_trace, int lane) {
+  constexpr int kUnroll = sizeof(IdxT) == 8 ? 8 : 16;
+  const IdxT* ip = static_cast<const IdxT*>(p.idx) + tok * p.topk;
+  int nv = 0;
+  for (int base = 0; base < p.topk; base += 32 * kUnroll) {
+    IdxT v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + u * 32 + lane;
+      v[u] = (j < p.topk) ? ip[j] : IdxT(-1);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + u * 32 + lane;
+      const bool ok = (j < p.topk) && slot_valid<IdxT>(v[u], p.num_kv);
+      const int row = ok ? static_cast<int>(v[u]) : -1;   // exact: num_kv < 2^31
+      const unsigned ball = __ballot_sync(0xffffffffu, ok);
+      if (ok) rows[nv + __popc(ball & ((1u << lane) - 1u))] = row;
+      if (write_trace && j < p.topk) p.trace[tok * p.topk + j] = row;
+      nv += __popc(ball);
+    }
+  }
+  __syncwarp();
+  return nv;
+}
+
+template <typename IdxT>
+__device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q,
+                              const CUtensorMap* tm_kv, uint8_t* base, Bars* b, uint32_t rank,
+                              int lane) {
+  const uint32_t sbase = smem_u32(base);
+  int* rows = reinterpret_cast<int*>(base + kRowsOff);
+  const int64_t cid = cluster_id_x(), ncl = nclusters_x();
+  uint32_t gt = 0, qn = 0;
+  int it = 0;
+  bool ok = true;
+  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
+    const int nv = compact_token<IdxT>(p, tok, rows, p.trace != nullptr && rank == 0, lane);
+    const int slot = it & 1;
+    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_empty[slot]),
+                                                 ((it >> 1) & 1) ^ 1, b, p.err, 1u));
+    if (!ok) break;
+    if (lane == 0) {
+      b->nvalid[slot] = nv;
+      mbar_arrive(bar_addr(b->meta_full[slot]));
+    }
+    if (nv == 0) continue;
+    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->q_empty), (qn & 1) ^ 1, b, p.err, 1u));
+    if (!ok) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(b->q_full), kQBytes);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb)
+        tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 64 * cb,
+                    static_cast<int>(tok * 128), bar_addr(b->q_full));
+    }
+    ++qn;
+    const int ntiles = (nv + kTileN - 1) / kTileN;
+    for (int j = 0; j < ntiles; ++j, ++gt) {
+      const uint32_t s = gt % kStages, ph = (gt / kStages) & 1;
+      ok = __all_sync(0xffffffffu,
+                      wait_bar<false>(bar_addr(b->kv_empty[s]), ph ^ 1, b, p.err, 1u));
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar_addr(b->kv_full[s]), kStageBytes);
+      __syncwarp();
+      const int first = rows[j * kTileN];   // the tile's first slot is always valid
+#pragma unroll
+      for (int k = lane; k < 64; k += 32) {
+        const int g = k >> 2, cb = k & 3;   // 16 groups of 4 rows x 4 column blocks
+        const int sl = j * kTileN + g * 4;
+        const int r0 = sl + 0 < nv ? rows[sl + 0] : first;
+        const int r1 = sl + 1 < nv ? rows[sl + 1] : first;
+        const int r2 = sl + 2 < nv ? rows[sl + 2] : first;
+        const int r3 = sl + 3 < nv ? rows[sl + 3] : first;
+        tma_gather4(sbase + kKVOff + s * kStageBytes + cb * 8192 + g * 512, tm_kv,
+                    256 * int(rank) + 64 * cb, r0, r1, r2, r3, bar_addr(b->kv_full[s]));
+      }
+    }
+    __syncwarp();
+  }
+  // drain: every issued load must land before the CTA may exit
+  if (lane == 0) {
+    const uint32_t n = gt < kStages ? gt : kStages;
+    for (uint32_t k = 0; k < n; ++k) {
+      const uint32_t g = gt - 1 - k;
+      wait_bar<false, true>(bar_addr(b->kv_full[g % kStages]), (g / kStages) & 1, b, p.err, 1u);
+    }
+    if (qn > 0) wait_bar<false, true>(bar_addr(b->q_full), (qn - 1) & 1, b, p.err, 1u);
+  }
+}
+
+// Single thread (warp 1, lane 0): issues every tcgen05.mma of the CTA.
+//   S(g)  = Q_half . K_half(g)^T -> S buffer g%2 (M=128, N=64, K=256: 16 MMAs)
+//   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs)
+// issued as S(0), S(1), PV(0), S(2), PV(1), ... so the next tile's scores are
+// computed while the softmax works on the current one.
+__device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem) {
+  const uint32_t sbase = smem_u32(base);
+  const int64_t cid = cluster_id_x(), ncl = nclusters_x();
+  constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTileN, false, false);
+  constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
+  uint32_t gt = 0, qn = 0, on = 0;
+  int it = 0;
+
+  auto issue_pv = [&](uint32_t g, int j) -> bool {
+    const uint32_t s = g % kStages;
+    if (!wait_bar<false>(bar_addr(b->p_full), g & 1, b, p.err, 2u)) return false;
+    if (j == 0 && !wait_bar<false>(bar_addr(b->o_free), (on & 1) ^ 1, b, p.err, 2u)) return false;
+    tc_fence_after();
+    const uint32_t kv = sbase + kKVOff + s * kStageBytes;
+#pragma unroll
+    for (int kk = 0; kk < kTileN / 16; ++kk) {
+      const uint64_t a = sdesc_sw128(sbase + kPOff + kk * 32, 16, 1024);
+      // V as MN-major B: 64-column chunks 8 KB apart, 8-slot groups 1 KB apart
+      const uint64_t bd = sdesc_sw128(kv + kk * 16 * 128, 8192, 1024);
+      mma_bf16_ss(tmem, a, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+    }
+    mma_commit(bar_addr(b->kv_empty[s]));
+    mma_commit(bar_addr(b->pv_done));
+    return true;
+  };
+
+  bool ok = true;
+  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
+    const int slot = it & 1;
+    if (!(ok = wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1, b, p.err, 2u))) break;
+    const int nv = b->nvalid[slot];
+    mbar_arrive(bar_addr(b->meta_empty[slot]));
+    if (nv == 0) continue;
+    if (!(ok = wait_bar<false>(bar_addr(b->q_full), qn & 1, b, p.err, 2u))) break;
+    tc_fence_after();
+    const int ntiles = (nv + kTileN - 1) / kTileN;
+    for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+      const uint32_t s = gt % kStages, ph = (gt / kStages) & 1;
+      const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
+      if (!(ok = wait_bar<false>(bar_addr(b->kv_full[s]), ph, b, p.err, 2u))) break;
+      if (!(ok = wait_bar<false>(bar_addr(b->s_free[sb]), sph ^ 1, b, p.err, 2u))) break;
+      tc_fence_after();
+      const uint32_t kv = sbase + kKVOff + s * kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const uint32_t koff = (kk & 3) * 32;   // 16 K elements = 32 B inside a 128 B row
+        const uint64_t a = sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + koff, 16, 1024);
+        const uint64_t bd = sdesc_sw128(kv + (kk >> 2) * 8192 + koff, 16, 1024);
+        mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_addr(b->s_full[sb]));
+      if (j == ntiles - 1) mma_commit(bar_addr(b->q_empty));
+      if (j > 0 && !(ok = issue_pv(gt - 1, j - 1))) break;
+    }
+    if (!ok) break;
+    if (!(ok = issue_pv(gt - 1, ntiles - 1))) break;
+    ++qn;
+    ++on;
+  }
+  // drain: every MMA issued must complete before TMEM is freed
+  mma_commit(bar_addr(b->drain));
+  wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
+}
+
+// Warps 2..5 (128 threads): thread = TMEM lane = head `row`.  Per tile: read
+// the partial S, swap it with the peer CTA, softmax, write P; per token: the
+// epilogue (sink fold, normalise, bf16 store of this CTA's half of O, lse).
+__device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
+                             uint32_t rank, int warp, int lane) {
+  const uint32_t sbase = smem_u32(base);
+  const int row = 32 * (warp & 3) + lane;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
+  const int64_t cid = cluster_id_x(), ncl = nclusters_x();
+  const uint32_t peer = rank ^ 1u;
+  const uint32_t x_mine = sbase + kXOff + row * 256;        // my row of the buffer the peer fills
+  const uint32_t x_peer = map_peer(x_mine, peer);           // my row of the peer's buffer
+  const uint32_t xfull_peer = map_peer(bar_addr(b->x_full), peer);
+  const uint32_t xfree_peer = map_peer(bar_addr(b->x_free), peer);
+  const float sl2 = p.scale * kLog2e;
+  const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
+  uint8_t* prow = base + kPOff + row * 128;
+  uint32_t gt = 0;
+  int it = 0;
+  bool ok = true;
+
+  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
+    const int slot = it & 1;
+    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1,
+                                                 b, p.err, 4u));
+    if (!ok) break;
+    const int nv = b->nvalid[slot];
+    mbar_arrive(bar_addr(b->meta_empty[slot]));
+    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
+                                           256 * rank);
+    if (nv == 0) {   // nothing valid: O = 0; lse = sink (finite) or -inf
+#pragma unroll
+      for (int c = 0; c < 32; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (rank == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
+      continue;
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    const int ntiles = (nv + kTileN - 1) / kTileN;
+    for (int j = 0; j < ntiles; ++j, ++gt) {
+      const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
+      ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]), sph, b, p.err, 4u));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(tl + kTmemS + sb * kTileN, sv);
+      tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_addr(b->s_free[sb]));
+
+      // swap partial scores with the peer: my partial -> its buffer, its partial <- mine
+      ok = __all_sync(0xffffffffu,
+                      wait_bar<true>(bar_addr(b->x_free), (gt & 1) ^ 1, b, p.err, 4u));
+      if (!ok) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_cluster_v4(x_peer + ((c ^ (row & 15)) << 4), __uint_as_float(sv[4 * c]),
+                      __uint_as_float(sv[4 * c + 1]), __uint_as_float(sv[4 * c + 2]),
+                      __uint_as_float(sv[4 * c + 3]));
+      mbar_arrive_remote(xfull_peer);
+      ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full), gt & 1, b, p.err, 4u));
+      if (!ok) break;
+      float s[64];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(base + kXOff + row * 256 +
+                                                          ((c ^ (row & 15)) << 4));
+        s[4 * c + 0] = __uint_as_float(sv[4 * c + 0]) + v.x;
+        s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + v.y;
+        s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + v.z;
+        s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + v.w;
+      }
+      mbar_arrive_remote(xfree_peer);
+
+      // online softmax, base 2; columns past the valid count are -inf
+      const int nvt = min(kTileN, nv - j * kTileN);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
+      const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m_run - mx);
+        m_run = mx;
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        s[i] = ex2(s[i] - m_run);
+        sum += s[i];
+      }
+      l_run = l_run * alpha + sum;
+
+      // the previous P.V must be done before P is overwritten or O rescaled
+      if (gt > 0) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bar<false>(bar_addr(b->pv_done), (gt - 1) & 1, b, p.err, 4u));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tl + 32 * c, o);
+        }
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 w;
+        w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
+        w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
+        w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
+        w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = w;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_addr(b->p_full));
+    }
+    if (!ok) break;
+
+    // epilogue: wait for the last P.V, fold the sink, normalise, store
+    ok = __all_sync(0xffffffffu,
+                    wait_bar<false>(bar_addr(b->pv_done), (gt - 1) & 1, b, p.err, 4u));
+    if (!ok) break;
+    tc_fence_after();
+    float m2 = m_run, l2 = l_run;
+    if (sk != -INFINITY) {
+      m2 = fmaxf(m_run, sk);
+      l2 = l_run * ex2(m_run - m2) + ex2(sk - m2);
+    }
+    const float f = ex2(m_run - m2) / l2;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tl + 32 * c, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * f, __uint_as_float(o[8 * q + 1]) * f);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * f, __uint_as_float(o[8 * q + 3]) * f);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * f, __uint_as_float(o[8 * q + 5]) * f);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * f, __uint_as_float(o[8 * q + 7]) * f);
+        orow[4 * c + q] = w;
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar_addr(b->o_free));
+    if (rank == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
+  }
+}
+
+template <typename IdxT>
+__global__ void __launch_bounds__(kThreads, 1)
+    h128_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_kv, const H128Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Bars* b = reinterpret_cast<Bars*>(base + kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_addr(b->q_full), 1);
+    mbar_init(bar_addr(b->q_empty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_addr(b->kv_full[s]), 1);
+      mbar_init(bar_addr(b->kv_empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_addr(b->s_full[i]), 1);
+      mbar_init(bar_addr(b->s_free[i]), 128);
+      mbar_init(bar_addr(b->meta_full[i]), 1);
+      mbar_init(bar_addr(b->meta_empty[i]), 1 + 128);
+    }
+    mbar_init(bar_addr(b->p_full), 128);
+    mbar_init(bar_addr(b->pv_done), 1);
+    mbar_init(bar_addr(b->x_full), 128);
+    mbar_init(bar_addr(b->x_free), 128);
+    mbar_init(bar_addr(b->o_free), 128);
+    mbar_init(bar_addr(b->drain), 1);
+    b->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_kv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&b->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();   // the peer's barriers are initialised before any remote arrive
+  const uint32_t tmem = b->tmem_base;
+
+  if (warp == 0) {
+    producer_role<IdxT>(p, &tm_q, &tm_kv, base, b, rank, lane);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role(p, base, b, tmem);
+    __syncwarp();
+  } else {
+    softmax_role(p, base, b, tmem, rank, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // no remote store or arrive may target an exited CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a [rows, 512] row-major matrix, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DeviceState {
+  bool ready = false;
+  int max_clusters = 0;
+};
+
+template <typename IdxT>
+cudaError_t prepare(DeviceState& st) {
+  auto kern = h128_fwd_kernel<IdxT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n <= 0) return cudaErrorInvalidConfiguration;
+  st.max_clusters = n;
+  st.ready = true;
+  return cudaSuccess;
+}
+
+template <typename IdxT>
+cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
+  constexpr int kMaxDev = 64;
+  static DeviceState states[kMaxDev];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!states[dev].ready && (e = prepare<IdxT>(states[dev])) != cudaSuccess) return e;
+  }
+  CUtensorMap tq, tkv;
+  if (!make_map(&tq, fp.q, static_cast<uint64_t>(fp.T) * 128, 64, 128) ||
+      !make_map(&tkv, fp.kv, static_cast<uint64_t>(fp.num_kv), 64, 1))
+    return cudaErrorInvalidValue;
+  unsigned int* err = nullptr;
+  if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_h128_error)) != cudaSuccess)
+    return e;
+  H128Params p;
+  p.idx = fp.idx;
+  p.sink = fp.sink;
+  p.out = static_cast<__nv_bfloat16*>(fp.out);
+  p.lse = fp.lse;
+  p.trace = fp.trace;
+  p.err = err;
+  p.T = fp.T;
+  p.num_kv = fp.num_kv;
+  p.topk = fp.topk;
+  p.idx64 = fp.idx64;
+  p.scale = fp.scale;
+
+  const int64_t clusters = fp.T < states[dev].max_clusters ? fp.T : states[dev].max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, h128_fwd_kernel<IdxT>, tq, tkv, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool h128_supported(int64_t T, int32_t H, int32_t topk, int64_t num_kv) {
+  return H == 128 && topk >= 1 && topk <= kMaxTopk && num_kv >= 1 && T >= 1 &&
+         T < (int64_t(1) << 24);
+}
+
+int launch_h128(const FwdParams& p, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = p.idx64 ? launch_typed<int64_t>(p, s) : launch_typed<int32_t>(p, s);
+  return static_cast<int>(e);
+}
 
 int h128_error_word(unsigned int** addr) {
-  *addr = nullptr;
-  return 0;
+  return static_cast<int>(cudaGetSymbolAddress(reinterpret_cast<void**>(addr), g_h128_error));
 }
 
 }  // namespace smla

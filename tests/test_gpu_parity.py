@@ -75,9 +75,13 @@ def _tiny_x(seed=0, sink=True, **cfg_kw):
     return cfg, synth.make_inputs(cfg)
 
 
+HEADS = [16, 128]   # the small-head kernel and the tcgen05 H = 128 kernel
+
+
+@pytest.mark.parametrize("H", HEADS)
 @pytest.mark.parametrize("variant", ["shuffled", "dups", "oob32", "oob64", "nosink", "sinkneg"])
-def test_tiny_variants(B, variant):
-    cfg, x = _tiny_x(seed=31, sink=(variant != "nosink"))
+def test_tiny_variants(B, variant, H):
+    cfg, x = _tiny_x(seed=31, sink=(variant != "nosink"), H=H)
     if variant == "shuffled":
         x["idx"] = synth.shuffle_rows(x["idx"], 1)
     elif variant == "dups":
@@ -93,18 +97,20 @@ def test_tiny_variants(B, variant):
     compare(out, lse, O, L)
 
 
+@pytest.mark.parametrize("H", HEADS)
 @pytest.mark.parametrize("dtype", [np.int32, np.int64])
 @pytest.mark.parametrize("splits", [0, 1, 3])
-def test_read_trace_bit_exact(B, dtype, splits):
-    cfg, x = _tiny_x(seed=5)
+def test_read_trace_bit_exact(B, dtype, splits, H):
+    cfg, x = _tiny_x(seed=5, H=H)
     x["idx"] = synth.inject_out_of_range(x["idx"].astype(dtype), cfg.num_kv, 9, frac=0.35)
     out, lse, tr = _run(B, x, splits=splits, trace=True)
     want = np.where(orc.valid_slots(x["idx"], cfg.num_kv), x["idx"].astype(np.int64), -1)
     np.testing.assert_array_equal(tr.cpu().numpy(), want)
 
 
-def test_poisoned_rows_and_guard_never_read(B):
-    cfg, x = _tiny_x(seed=6)
+@pytest.mark.parametrize("H", HEADS)
+def test_poisoned_rows_and_guard_never_read(B, H):
+    cfg, x = _tiny_x(seed=6, H=H)
     idx = x["idx"].copy()
     idx[idx == 0] = -1
     used = np.unique(idx[(idx >= 0) & (idx < cfg.num_kv)])
@@ -118,9 +124,10 @@ def test_poisoned_rows_and_guard_never_read(B):
     compare(out, lse, O, L)
 
 
+@pytest.mark.parametrize("H", HEADS)
 @pytest.mark.parametrize("sink", [True, False])
-def test_all_invalid_rows(B, sink):
-    cfg, x = _tiny_x(seed=7, sink=sink)
+def test_all_invalid_rows(B, sink, H):
+    cfg, x = _tiny_x(seed=7, sink=sink, H=H)
     x["idx"] = np.full_like(x["idx"], -1)
     x["idx"][::3, 5] = cfg.num_kv
     x["idx"][1::4, 0] = 2 ** 31 - 1
@@ -133,8 +140,9 @@ def test_all_invalid_rows(B, sink):
         assert np.all(np.isneginf(L))
 
 
-def test_mixed_empty_and_full_rows(B):
-    cfg, x = _tiny_x(seed=8)
+@pytest.mark.parametrize("H", HEADS)
+def test_mixed_empty_and_full_rows(B, H):
+    cfg, x = _tiny_x(seed=8, H=H)
     x["idx"][::2] = -1                      # every other token fully masked
     for splits in (0, 1, 4):
         out, lse, _ = _run(B, x, splits=splits)
@@ -174,17 +182,21 @@ def test_head_counts(B, H):
     compare(out, lse, O, L)
 
 
-@pytest.mark.parametrize("topk,window", [(1, 1), (3, 2), (67, 40), (130, 64), (2500, 200)])
-def test_ragged_topk(B, topk, window):
-    cfg = synth.CONFIGS["tiny"].with_(T=150, pool=600, ratio=1, topk=topk, window=window, seed=13)
+@pytest.mark.parametrize("H", HEADS)
+@pytest.mark.parametrize("topk,window", [(1, 1), (3, 2), (67, 40), (130, 64), (2048, 150),
+                                         (2500, 200)])
+def test_ragged_topk(B, topk, window, H):
+    cfg = synth.CONFIGS["tiny"].with_(T=150, H=H, pool=2400, ratio=1, topk=topk, window=window,
+                                      seed=13)
     x = synth.make_inputs(cfg)
     out, lse, _ = _run(B, x)
     O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
     compare(out, lse, O, L)
 
 
-def test_topk_zero_and_empty_pool(B):
-    cfg, x = _tiny_x(seed=14)
+@pytest.mark.parametrize("H", HEADS)
+def test_topk_zero_and_empty_pool(B, H):
+    cfg, x = _tiny_x(seed=14, H=H)
     x0 = dict(x, idx=np.zeros((cfg.T, 0), dtype=np.int32))
     out, lse, _ = _run(B, x0)
     assert torch.all(out == 0)
@@ -196,16 +208,18 @@ def test_topk_zero_and_empty_pool(B):
     assert torch.all(out == 0)
 
 
-def test_single_token(B):
-    cfg, x = _tiny_x(seed=15)
+@pytest.mark.parametrize("H", HEADS)
+def test_single_token(B, H):
+    cfg, x = _tiny_x(seed=15, H=H)
     x1 = dict(x, q=x["q"][40:41], idx=x["idx"][40:41])
     out, lse, _ = _run(B, x1)
     O, L = orc.sparse_mla_fwd(x1["q"], x1["kv"], x1["idx"], x1["sink"], x1["scale"])
     compare(out, lse, O, L)
 
 
-def test_out_buffer_bit_identical_to_allocating_call(B):
-    cfg, x = _tiny_x(seed=16)
+@pytest.mark.parametrize("H", HEADS)
+def test_out_buffer_bit_identical_to_allocating_call(B, H):
+    cfg, x = _tiny_x(seed=16, H=H)
     q, kv, idx, sink, _ = to_dev(x, DEV)
     o1, l1 = B.sparse_mla_fwd(q, kv, idx, sink, x["scale"])
     out = torch.full_like(q, float("nan"))
@@ -235,10 +249,38 @@ def test_binding_rejections(B):
         B.sparse_mla_fwd(q, kv, idx, sink, scale=float("nan"))
 
 
-def test_deterministic(B):
-    cfg = synth.CONFIGS["sweep_k256"].with_(T=512)
+@pytest.mark.parametrize("name", ["sweep_k256", "h128"])
+def test_deterministic(B, name):
+    cfg = synth.CONFIGS[name].with_(T=512)
     x = synth.make_inputs(cfg)
     a, la, _ = _run(B, x)
     b, lb, _ = _run(B, x)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(la.view(torch.int32), lb.view(torch.int32))
+
+
+def test_h128_uses_tcgen05_kernel(B):
+    assert B.sparse_mla_plan(4096, 128, 512) == (1, 1, 1)
+    assert B.sparse_mla_plan(8192, 128, 1024) == (1, 1, 1)
+    assert B.sparse_mla_plan(64, 128, 2500)[0] == 0      # beyond its row list: split path
+
+
+@pytest.mark.parametrize("T", [1, 2, 75, 77, 153, 1000])
+def test_h128_token_counts(B, T):
+    # fewer tokens than clusters, one per cluster, several per persistent cluster
+    cfg = synth.CONFIGS["h128"].with_(T=T, pool=max(8, T // 4), seed=40 + T)
+    x = synth.make_inputs(cfg)
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+def test_h128_vs_split_path(B):
+    cfg = synth.CONFIGS["h128"].with_(T=300, seed=41)
+    x = synth.make_inputs(cfg)
+    o1, l1, _ = _run(B, x, splits=0)     # tcgen05 kernel
+    o2, l2, _ = _run(B, x, splits=2)     # small-head kernel, split-TOPK + combine
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+    fin = torch.isfinite(l1)
+    assert torch.equal(fin, torch.isfinite(l2))
+    assert (l1[fin] - l2[fin]).abs().max().item() <= 5e-3
