@@ -281,6 +281,8 @@ def run_ours(args, cfg) -> None:
     all_flops = sdist.sum_over_ranks(counts.flops, dev)
     value = all_flops * K / (max_total_ms * 1e-3) / 1e12
 
+    geom = B.sparse_mla_launch_config(cfg.T, cfg.H, cfg.topk, cfg.num_kv)
+
     # end to end through the public call: pinned host inputs in, results out, every step
     E = args.e2e_steps
     hq = torch.from_numpy(x["q"].view(np.int16)).pin_memory()
@@ -301,26 +303,28 @@ def run_ours(args, cfg) -> None:
         ho.copy_(out, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(E)]
-    sdist.barrier(dev)
-    for k in range(E):
-        flush.zero_()
-        eev[k][0].record(stream)
-        e2e_step()
-        eev[k][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sdist.max_over_ranks(sum(a.elapsed_time(b) for a, b in eev), dev)
     h2d = (hq.numel() * 2 + hkv.numel() * 2 + hidx.numel() * hidx.element_size() +
            (hsink.numel() * 4 if hsink is not None else 0))
     d2h = ho.numel() * 2 + hl.numel() * 4
-    e2e = {"value": all_flops * E / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "ms_per_step": e2e_ms / E, "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(d2h), "steps": E,
-           "path": "binding.sparse_mla_fwd (C ABI) with pinned host buffers"}
+    e2e = None
+    if E > 0:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(E)]
+        sdist.barrier(dev)
+        for k in range(E):
+            flush.zero_()
+            eev[k][0].record(stream)
+            e2e_step()
+            eev[k][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sdist.max_over_ranks(sum(a.elapsed_time(b) for a, b in eev), dev)
+        e2e = {"value": all_flops * E / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms / E, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": E,
+               "path": "binding.sparse_mla_fwd (C ABI) with pinned host buffers"}
 
     # roofline of the dominant kernel (one launch per step when splits == 1)
     peaks, psrc = roofline.load_peaks(ROOT)
@@ -343,12 +347,13 @@ def run_ours(args, cfg) -> None:
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; window + causally visible pool top-k; bf16 N(0,1))",
             "config": config_dict(cfg, counts, {"kernel_family": family, "splits": splits,
+                                                "launch": geom,
                                                 "parallelism": f"replicas x{world} (own batch per rank)"}),
             "e2e": e2e, "gpu_launches": K * launches, "clocks": clocks, "roofline": roof,
             "roofline_terms": t,
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
                         "max": max(step_ms)}}
-    if world == 1 and rank == 0:
+    if world == 1 and rank == 0 and args.cpu_seconds > 0:
         r = oracle_rate(x, cfg, args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": r["tflops"], "unit": "TFLOP/s", "cores": _blas_threads(), "kind": "oracle",

@@ -113,6 +113,18 @@ smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_sp
                               int32_t* launches_out);
 
 /*
+ * sparse_mla_launch_config -- the launch geometry sparse_mla_fwd_ex would use on
+ * the current device for these sizes (queries the device's occupancy, so it
+ * makes CUDA runtime calls but launches nothing).  Writes the CTAs of the
+ * main kernel's grid, threads per CTA, CTAs per cluster and dynamic shared
+ * memory bytes per CTA.  Any output pointer may be NULL.
+ */
+smla_status_t sparse_mla_launch_config(int64_t T, int32_t H, int32_t topk, int64_t num_kv,
+                                       int32_t num_splits, int32_t* grid_ctas,
+                                       int32_t* cta_threads, int32_t* cluster_size,
+                                       int32_t* smem_bytes);
+
+/*
  * sparse_mla_device_status -- synchronises `stream`, then reads and clears
  * the library's device error word on the current device.  Returns
  * SMLA_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait since the last

@@ -38,6 +38,7 @@ SIGNATURES = {
     "sparse_mla_fwd": (_I32, _FWD_ARGS),
     "sparse_mla_fwd_ex": (_I32, _FWD_ARGS + [_I32, _P]),
     "sparse_mla_plan": (_I32, [_I64, _I32, _I32, _I32, _P, _P, _P]),
+    "sparse_mla_launch_config": (_I32, [_I64, _I32, _I32, _I64, _I32, _P, _P, _P, _P]),
     "sparse_mla_device_status": (_I32, [_P]),
     "sparse_mla_strerror": (ctypes.c_char_p, [_I32]),
     "sparse_mla_last_cuda_error": (ctypes.c_char_p, []),
@@ -94,6 +95,16 @@ def sparse_mla_plan(T: int, H: int, topk: int, num_splits: int = 0):
     if st != SMLA_OK:
         raise SparseMLAError(st, "sparse_mla_plan")
     return fam.value, sp.value, ln.value
+
+
+def sparse_mla_launch_config(T: int, H: int, topk: int, num_kv: int, num_splits: int = 0):
+    """Launch geometry on the current device: dict(grid_ctas, threads, cluster, smem)."""
+    v = [ctypes.c_int32() for _ in range(4)]
+    st = lib().sparse_mla_launch_config(T, H, topk, num_kv, num_splits,
+                                        *[ctypes.byref(x) for x in v])
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_launch_config")
+    return dict(zip(("grid_ctas", "threads", "cluster", "smem"), (x.value for x in v)))
 
 
 def _stream_ptr(stream) -> int:

@@ -202,6 +202,26 @@ smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_sp
   return SMLA_OK;
 }
 
+smla_status_t sparse_mla_launch_config(int64_t T, int32_t H, int32_t topk, int64_t num_kv,
+                                       int32_t num_splits, int32_t* grid_ctas,
+                                       int32_t* cta_threads, int32_t* cluster_size,
+                                       int32_t* smem_bytes) {
+  if (T < 0 || topk < 0 || num_kv < 0) return SMLA_ERR_BAD_SHAPE;
+  if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
+  Plan pl;
+  smla_status_t st = make_plan(T, H, topk, num_kv, num_splits, &pl);
+  if (st != SMLA_OK) return st;
+  smla::LaunchGeom g{0, 0, 0, 0};
+  const int e = pl.family == 1 ? smla::h128_geometry(T, &g)
+                               : smla::smallh_geometry(T, H, pl.splits, &g);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "launch geometry");
+  if (grid_ctas) *grid_ctas = g.grid_ctas;
+  if (cta_threads) *cta_threads = g.threads;
+  if (cluster_size) *cluster_size = g.cluster;
+  if (smem_bytes) *smem_bytes = g.smem;
+  return SMLA_OK;
+}
+
 smla_status_t sparse_mla_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

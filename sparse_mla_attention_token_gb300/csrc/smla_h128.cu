@@ -578,19 +578,29 @@ cudaError_t prepare(DeviceState& st) {
   return cudaSuccess;
 }
 
+constexpr int kMaxDev = 64;
+
+// Per-device, per-instantiation launch state (shared-memory attribute set,
+// co-resident cluster count), prepared on first use.
 template <typename IdxT>
-cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
-  constexpr int kMaxDev = 64;
+cudaError_t device_state(DeviceState** out) {
   static DeviceState states[kMaxDev];
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!states[dev].ready && (e = prepare<IdxT>(states[dev])) != cudaSuccess) return e;
-  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!states[dev].ready && (e = prepare<IdxT>(states[dev])) != cudaSuccess) return e;
+  *out = &states[dev];
+  return cudaSuccess;
+}
+
+template <typename IdxT>
+cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  cudaError_t e = device_state<IdxT>(&st);
+  if (e != cudaSuccess) return e;
   CUtensorMap tq, tkv;
   if (!make_map(&tq, fp.q, static_cast<uint64_t>(fp.T) * 128, 64, 128) ||
       !make_map(&tkv, fp.kv, static_cast<uint64_t>(fp.num_kv), 64, 1))
@@ -611,7 +621,7 @@ cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   p.idx64 = fp.idx64;
   p.scale = fp.scale;
 
-  const int64_t clusters = fp.T < states[dev].max_clusters ? fp.T : states[dev].max_clusters;
+  const int64_t clusters = fp.T < st->max_clusters ? fp.T : st->max_clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -640,6 +650,18 @@ int launch_h128(const FwdParams& p, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = p.idx64 ? launch_typed<int64_t>(p, s) : launch_typed<int32_t>(p, s);
   return static_cast<int>(e);
+}
+
+int h128_geometry(int64_t T, LaunchGeom* g) {
+  DeviceState* st = nullptr;
+  const cudaError_t e = device_state<int32_t>(&st);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  const int64_t clusters = T < st->max_clusters ? T : st->max_clusters;
+  g->grid_ctas = static_cast<int>(2 * clusters);
+  g->threads = kThreads;
+  g->cluster = 2;
+  g->smem = static_cast<int>(kSmemBytes);
+  return 0;
 }
 
 int h128_error_word(unsigned int** addr) {

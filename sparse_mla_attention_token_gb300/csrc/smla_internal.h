@@ -44,6 +44,16 @@ bool h128_supported(int64_t T, int32_t H, int32_t topk, int64_t num_kv);
 // Device address of the h128 kernel's error word (bounded waits), or nullptr.
 int h128_error_word(unsigned int** addr);
 
+// Launch geometry of each kernel family: grid CTAs, threads, cluster size, smem.
+struct LaunchGeom {
+  int grid_ctas;
+  int threads;
+  int cluster;
+  int smem;
+};
+int smallh_geometry(int64_t T, int32_t H, int32_t splits, LaunchGeom* g);
+int h128_geometry(int64_t T, LaunchGeom* g);
+
 // Merge split partials into out / lse, folding the sink once.
 int launch_combine(const FwdParams& p, void* stream);
 

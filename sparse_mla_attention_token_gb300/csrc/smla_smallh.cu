@@ -315,6 +315,14 @@ cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+int smallh_geometry(int64_t T, int32_t H, int32_t splits, LaunchGeom* g) {
+  g->grid_ctas = static_cast<int>(T * ((H + kHG - 1) / kHG) * splits);
+  g->threads = kThreads;
+  g->cluster = 1;
+  g->smem = static_cast<int>(sizeof(Smem)) + 1024;
+  return 0;
+}
+
 int launch_smallh(const FwdParams& p, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool split = p.splits > 1;

@@ -87,6 +87,9 @@ CONFIGS = {
     "h128": Config("h128", T=4096, H=128, pool=1024, ratio=4, topk=512, window=128, seed=3),
     "h128_long": Config("h128_long", T=8192, H=128, pool=1024, ratio=8, topk=1024, window=256,
                         index_dtype="int64", kv_offset_bytes=(2 << 30) + 4096, seed=4),
+    # the h128 recipe at a quarter of the tokens: the small case for Nsight Compute captures
+    "h128_small": Config("h128_small", T=1024, H=128, pool=256, ratio=4, topk=512, window=128,
+                         seed=3),
 }
 
 # The workload the headline metric is quoted on (T=4096 H=128 topk=512).
