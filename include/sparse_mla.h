@@ -54,7 +54,8 @@ typedef enum {
   SMLA_ERR_ALIASING = 7,         /* out or lse overlaps an input                     */
   SMLA_ERR_CUDA = 8,             /* a CUDA runtime call failed (see _last_cuda_error)*/
   SMLA_ERR_DEVICE_TIMEOUT = 9,   /* a kernel's bounded wait expired (device status)  */
-  SMLA_ERR_BAD_SPLITS = 10       /* forced split count out of range                  */
+  SMLA_ERR_BAD_SPLITS = 10,      /* forced split count out of range                  */
+  SMLA_ERR_SCRATCH_LIMIT = 11    /* splits*T*H beyond the library's static scratch   */
 } smla_status_t;
 
 /*
@@ -101,6 +102,38 @@ smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_
                                 void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
                                 int32_t topk, void* stream, int32_t num_splits,
                                 int64_t* read_trace);
+
+/*
+ * sparse_mla_fwd_static_scratch -- the split-TOPK path without any allocation.
+ *
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that must not allocate device memory while they run: code executing under a
+ * CUDA stream capture that must not add allocation nodes, serving loops with a
+ * fixed memory budget, and hosts whose allocator is owned by another runtime.
+ * sparse_mla_fwd_ex allocates the split path's partial results on every call;
+ * this entry point keeps them in one fixed array inside the library instead
+ * (16 MiB of device memory, held by every GPU that loads the library until the
+ * process exits) and calls no cudaMalloc / cudaFree or any allocating routine.
+ *
+ *   Arguments and results: as sparse_mla_fwd (same layouts, same validation).
+ *   num_splits   0 = the library's split count (at least 2); otherwise 2..64.
+ *   Limit        num_splits * T * H <= 8192 partial rows, else
+ *                SMLA_ERR_SCRATCH_LIMIT before any CUDA call.  This suits
+ *                decode-sized calls (a few tokens); larger calls belong on
+ *                sparse_mla_fwd.
+ *   First call   on each device looks up the array's device address once;
+ *                make it before any stream capture.
+ *   Sharing      every call uses the same array: calls whose kernels overlap
+ *                on the GPU (other streams, other host threads) race and give
+ *                wrong results.  Serialise them on one stream.  No state
+ *                carries over between calls: every partial row a call reads,
+ *                it wrote first.
+ */
+smla_status_t sparse_mla_fwd_static_scratch(const void* q, const void* kv,
+                                            const void* topk_indices, int32_t index_dtype,
+                                            const float* attn_sink, float scale, void* out,
+                                            float* lse, int64_t T, int32_t H, int64_t num_kv,
+                                            int32_t topk, void* stream, int32_t num_splits);
 
 /*
  * sparse_mla_plan -- what sparse_mla_fwd_ex would launch, without launching.

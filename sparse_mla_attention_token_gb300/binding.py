@@ -28,7 +28,7 @@ STATUS = {
     0: "SMLA_OK", 1: "SMLA_ERR_NULL_PTR", 2: "SMLA_ERR_BAD_SHAPE", 3: "SMLA_ERR_UNSUPPORTED_H",
     4: "SMLA_ERR_BAD_INDEX_DTYPE", 5: "SMLA_ERR_MISALIGNED", 6: "SMLA_ERR_BAD_SCALE",
     7: "SMLA_ERR_ALIASING", 8: "SMLA_ERR_CUDA", 9: "SMLA_ERR_DEVICE_TIMEOUT",
-    10: "SMLA_ERR_BAD_SPLITS",
+    10: "SMLA_ERR_BAD_SPLITS", 11: "SMLA_ERR_SCRATCH_LIMIT",
 }
 
 # exported symbol -> (restype, argtypes)
@@ -37,6 +37,7 @@ _FWD_ARGS = [_P, _P, _P, _I32, _P, _F32, _P, _P, _I64, _I32, _I64, _I32, _P]
 SIGNATURES = {
     "sparse_mla_fwd": (_I32, _FWD_ARGS),
     "sparse_mla_fwd_ex": (_I32, _FWD_ARGS + [_I32, _P]),
+    "sparse_mla_fwd_static_scratch": (_I32, _FWD_ARGS + [_I32]),
     "sparse_mla_plan": (_I32, [_I64, _I32, _I32, _I32, _P, _P, _P]),
     "sparse_mla_launch_config": (_I32, [_I64, _I32, _I32, _I64, _I32, _P, _P, _P, _P]),
     "sparse_mla_device_status": (_I32, [_P]),
@@ -198,3 +199,49 @@ def sparse_mla_device_status(stream=None) -> int:
     import torch
     return int(lib().sparse_mla_device_status(_stream_ptr(stream) if torch.cuda.is_available()
                                               else None))
+
+
+def sparse_mla_fwd_static_scratch(q, kv, topk_indices, out, lse, attn_sink=None,
+                                  scale: Optional[float] = None, num_splits: int = 0,
+                                  stream=None):
+    """The split-TOPK forward with no device allocation at all; returns ``(out, lse)``.
+
+    For callers that may not allocate while they run (a stream being
+    captured, a fixed memory budget, an allocator owned by someone else):
+    ``out`` and ``lse`` must be passed in, and the split partials live in the
+    library's own 16 MiB static array.  ``num_splits * T * H`` may not exceed
+    8192.  Calls that overlap on the GPU share that array and race; run them
+    on one stream.  The first call on a device sets up the array's address.
+    """
+    import torch
+    if q.dtype != torch.bfloat16 or kv.dtype != q.dtype:
+        raise RuntimeError(f"q and kv must be bfloat16, got {q.dtype} / {kv.dtype}")
+    if topk_indices.dtype not in (torch.int32, torch.int64):
+        raise RuntimeError(f"topk_indices must be int32 or int64, got {topk_indices.dtype}")
+    T, H, _ = q.shape
+    dev = q.device
+    for n, x in (("q", q), ("kv", kv), ("topk_indices", topk_indices), ("out", out), ("lse", lse)):
+        _check_dev(n, x, dev)
+        if not x.is_contiguous():
+            raise RuntimeError(f"{n} must be contiguous")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise RuntimeError("out must match q's shape and dtype")
+    if tuple(lse.shape) != (T, H) or lse.dtype != torch.float32:
+        raise RuntimeError(f"lse must be float32 [{T}, {H}]")
+    if attn_sink is not None:
+        _check_dev("attn_sink", attn_sink, dev)
+        if attn_sink.dtype != torch.float32 or tuple(attn_sink.shape) != (H,):
+            raise RuntimeError(f"attn_sink must be float32 [{H}]")
+    if scale is None:
+        scale = 512 ** -0.5
+    idt = SMLA_IDX_INT64 if topk_indices.dtype == torch.int64 else SMLA_IDX_INT32
+    with torch.cuda.device(dev):
+        st = lib().sparse_mla_fwd_static_scratch(
+            q.data_ptr(), kv.data_ptr() if kv.numel() else None,
+            topk_indices.data_ptr() if topk_indices.numel() else None, idt,
+            attn_sink.data_ptr() if attn_sink is not None else None, float(scale),
+            out.data_ptr(), lse.data_ptr(), T, H, kv.shape[0], topk_indices.shape[1],
+            _stream_ptr(stream), int(num_splits))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_fwd_static_scratch")
+    return out, lse

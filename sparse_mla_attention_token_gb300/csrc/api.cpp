@@ -188,6 +188,41 @@ smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_
              stream, num_splits, read_trace);
 }
 
+smla_status_t sparse_mla_fwd_static_scratch(const void* q, const void* kv,
+                                            const void* topk_indices, int32_t index_dtype,
+                                            const float* attn_sink, float scale, void* out,
+                                            float* lse, int64_t T, int32_t H, int64_t num_kv,
+                                            int32_t topk, void* stream, int32_t num_splits) {
+  smla_status_t st = validate(q, kv, topk_indices, index_dtype, attn_sink, scale, out, lse, T, H,
+                              num_kv, topk, nullptr);
+  if (st != SMLA_OK) return st;
+  if (num_splits == 1) return SMLA_ERR_BAD_SPLITS;   // this path always splits
+  Plan pl;
+  st = make_plan(T, H, topk, num_kv, num_splits, &pl);
+  if (st != SMLA_OK) return st;
+  const int splits = std::max(2, pl.splits);
+  if (T == 0) return SMLA_OK;
+  if (int64_t(splits) * T * H > smla::kNoAllocScratchRows) return SMLA_ERR_SCRATCH_LIMIT;
+  smla::FwdParams p{};
+  p.q = q;
+  p.kv = kv;
+  p.idx = topk_indices;
+  p.sink = attn_sink;
+  p.out = out;
+  p.lse = lse;
+  p.trace = nullptr;
+  p.T = T;
+  p.num_kv = num_kv;
+  p.H = H;
+  p.topk = topk;
+  p.splits = splits;
+  p.idx64 = index_dtype == SMLA_IDX_INT64 ? 1 : 0;
+  p.scale = scale;
+  const int e = smla::launch_split_static_scratch(p, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "static-scratch split path launch");
+  return SMLA_OK;
+}
+
 smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_splits,
                               int32_t* kernel_family, int32_t* splits_out,
                               int32_t* launches_out) {
@@ -254,6 +289,9 @@ const char* sparse_mla_strerror(int32_t status) {
     case SMLA_ERR_CUDA: return "CUDA runtime error";
     case SMLA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (outputs unspecified)";
     case SMLA_ERR_BAD_SPLITS: return "split count out of range for this topk";
+    case SMLA_ERR_SCRATCH_LIMIT:
+      return "splits*T*H exceeds the 8192 partial rows of the static scratch "
+             "(use sparse_mla_fwd for calls this large)";
     default: return "unknown status";
   }
 }

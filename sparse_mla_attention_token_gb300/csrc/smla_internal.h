@@ -54,6 +54,13 @@ struct LaunchGeom {
 int smallh_geometry(int64_t T, int32_t H, int32_t splits, LaunchGeom* g);
 int h128_geometry(int64_t T, LaunchGeom* g);
 
+// Partial rows (splits * T * H) the static scratch of the allocation-free
+// split path holds: 8192 rows of 512 + 1 fp32 = 16 MiB.
+constexpr int64_t kNoAllocScratchRows = 8192;
+// Split path (splits >= 2) with its partials in the library's static scratch;
+// fills p.part_o / p.part_lse itself.  Returns a cudaError_t value.
+int launch_split_static_scratch(FwdParams p, void* stream);
+
 // Merge split partials into out / lse, folding the sink once.
 int launch_combine(const FwdParams& p, void* stream);
 

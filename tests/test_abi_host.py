@@ -47,7 +47,7 @@ def test_exports_every_declared_function(L):
 
 def test_abi_version_and_strerror(L):
     assert binding.abi_version() == 1
-    for code in range(0, 11):
+    for code in range(0, 12):
         s = binding.strerror(code)
         assert s and s != "unknown status"
     assert binding.strerror(999) == "unknown status"
@@ -98,3 +98,16 @@ def test_plan(L):
     assert binding.sparse_mla_plan(0, 16, 64)[2] == 0
     with pytest.raises(binding.SparseMLAError):
         binding.sparse_mla_plan(4096, 16, 5000, 1)
+
+
+def test_static_scratch_entry_validates_before_cuda(L):
+    f = L.sparse_mla_fwd_static_scratch
+    args = [Q, KV, IDX, 0, SINK, 0.04, OUT, LSE]
+    # 8192 partial rows at most: 2 splits x 300 tokens x 16 heads is over
+    assert f(*args, 300, 16, 80, 64, None, 2) == 11
+    assert f(*args, 64, 128, 80, 64, None, 0) == 11        # 2 x 64 x 128 = 16384
+    assert f(*args, 4, 16, 80, 64, None, 1) == 10          # this path always splits
+    assert f(*args, 4, 16, 80, 64, None, 65) == 10
+    assert f(*args, 4, 12, 80, 64, None, 2) == 3
+    assert f(None, KV, IDX, 0, SINK, 0.04, OUT, LSE, 4, 16, 80, 64, None, 2) == 1
+    assert f(*args, 0, 16, 80, 64, None, 2) == 0           # T == 0: nothing to do
