@@ -54,6 +54,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Two floats -> packed fp16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Packed fp16x2 -> the two floats (exact).
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  float lo, hi;
+  asm("{\n.reg .f16 l, h;\nmov.b32 {l, h}, %2;\ncvt.f32.f16 %0, l;\ncvt.f32.f16 %1, h;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
+  return make_float2(lo, hi);
+}
+
 // The hardware base-2 exponential (MUFU.EX2): ex2.approx.ftz.f32.
 __device__ __forceinline__ float ex2(float x) {
   float y;

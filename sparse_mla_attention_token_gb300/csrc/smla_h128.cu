@@ -7,32 +7,37 @@
 // Why a CTA pair.  O[128 x 512] in fp32 is 256 KB, the whole tensor memory
 // of one SM, and S needs a 512-deep contraction.  Each CTA of the pair owns
 // one 256-wide half of the head dim (rank r: columns 256r..256r+255):
-//   * S_r = Q[:, half r] . K[:, half r]^T (partial over its half), the two
-//     partials exchanged through distributed shared memory (fp32) and summed
-//     as own + peer, which is bit-identical in both CTAs;
+//   * S_r = Q[:, half r] . K[:, half r]^T, its partial scores over that half;
+//   * the pair swaps partials: each CTA rounds its own partial to fp16, sends
+//     it with st.async (the bytes are counted on the peer's mbarrier, so no
+//     fence per thread is needed) and forms S = f16(S_0) + f16(S_1) in fp32,
+//     which is bit-identical in both CTAs;
 //   * both CTAs run the same online softmax on the same S;
 //   * O[:, half r] += P . V[:, half r] into its own TMEM.
 //   TMEM per CTA: O half 256 columns + two 64-column S buffers.
 //
-// Data movement.  The producer warp compacts the token's valid slots
+// Data movement.  Producer warp 0 compacts the token's valid slots
 // (0 <= idx < num_kv at the index's full width; PR #6002 "Invalid KV rows",
-// "int64 indices") into a row list, loads the token's Q half with 2-D TMA and
-// gathers 64 rows per tile with TMA gather4 (half rows, 512 B each) into a
-// 3-stage ring in the 128-byte-swizzled layout.  One tile serves as the
-// K-major B operand of Q.K^T and the MN-major B operand of P.V.  The ragged
-// tail of the last tile repeats a valid row (its scores are masked to -inf,
-// its probability is exactly 0), so no invalid slot is ever read.
+// "int64 indices") into a row list and loads the token's Q half with 2-D TMA.
+// Producer warps 0 and 1 gather 64 half rows (512 B each) per tile with
+// 16-byte cp.async straight into the 128-byte-swizzled layout of a 3-stage
+// ring; each thread fences its landed copies into the async proxy before it
+// arrives on the stage's barrier.  One tile serves as the K-major B operand of
+// Q.K^T and the MN-major B operand of P.V.  The ragged tail of a token's last
+// tile is zero-filled and its scores are masked: no invalid slot is read.
 //
-// Warp roles (192 threads): warp 0 producer, warp 1 TMEM owner and
-// single-thread MMA issuer, warps 2..5 softmax + epilogue (thread = TMEM lane =
-// head).  Softmax is base 2 with the sink folded once in the epilogue
+// Pipeline.  The MMA thread issues S(g+1) before P(g).V(g), across token
+// boundaries too; the softmax warps handle tile g-1 while tile g's score swap
+// is in flight.  Softmax is base 2 with the sink folded once in the epilogue
 // (m' = max(m, sink), l' = l 2^(m-m') + 2^(sink-m'), lse = ln2 (m' + log2 l'));
 // the running max is only raised when it grows by more than 2^8, which keeps
 // O rescales rare and is exact because O and l use the same stale max.
 //
-// Every mbarrier wait is bounded: on expiry the kernel sets an error word,
-// every role leaves its loop, in-flight copies and MMAs are drained with
-// bounded waits, TMEM is freed and the kernel returns.
+// Warps (224 threads): 0-1 producers, 2 TMEM owner + single-thread MMA issuer,
+// 3-6 softmax + epilogue (thread = TMEM lane = head).  Every mbarrier wait is
+// bounded: on expiry the kernel sets an error word, every role leaves its
+// loop, in-flight copies and MMAs are drained, TMEM is freed and the kernel
+// returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -49,7 +54,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kProducerThreads = 64;  // warps 0-1
+constexpr int kMmaWarp = 2;
 constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 3;
 constexpr int kMaxTopk = 2048;        // row-list capacity
@@ -63,9 +70,9 @@ constexpr uint32_t kKVOff = kQOff + kQBytes;          // [stage][4 col blocks][6
 constexpr uint32_t kStageBytes = kTileN * 256 * 2;    // 32 KB
 constexpr uint32_t kPOff = kKVOff + kStages * kStageBytes;   // [128 rows][128 B] bf16
 constexpr uint32_t kPBytes = 128 * kTileN * 2;        // 16 KB
-constexpr uint32_t kXOff = kPOff + kPBytes;           // peer's partial S: [128 rows][64 fp32]
-constexpr uint32_t kXBytes = 128 * kTileN * 4;        // 32 KB
-constexpr uint32_t kRowsOff = kXOff + kXBytes;        // int32 row list
+constexpr uint32_t kXOff = kPOff + kPBytes;           // peer partials: [2][128 rows][64 fp16]
+constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
+constexpr uint32_t kRowsOff = kXOff + 2 * kXBufBytes; // int32 row list
 constexpr uint32_t kBarOff = kRowsOff + kMaxTopk * 4;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024; // + barriers + alignment slack
 
@@ -76,11 +83,13 @@ struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, pv_done;
-  uint64_t x_full, x_free;
+  uint64_t x_full[2], x_free[2];
   uint64_t o_free;
   uint64_t meta_full[2], meta_empty[2];
   uint64_t drain;
   int nvalid[2];
+  int prod_nv;
+  int prod_stop;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -88,6 +97,7 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct H128Params {
   const void* idx;
+  const __nv_bfloat16* kv;
   const float* sink;
   __nv_bfloat16* out;
   float* lse;
@@ -156,94 +166,120 @@ __device__ __forceinline__ int compact_token(const H128Params& p, int64_t tok, i
   return nv;
 }
 
+// This thread's cp.async copies of a tile have landed (wait_group): make them
+// visible to the tensor core's async proxy, then count them on the barrier.
+__device__ __forceinline__ void land_and_arrive(uint32_t bar) {
+  fence_proxy_async_smem();
+  mbar_arrive(bar);
+}
+
+// Warps 0-1.  Warp 0 compacts the index list and loads Q (2-D TMA); both warps
+// gather the tile's half rows: warp w copies rows w, w+2, ..., lane c copies
+// 16-byte chunk c of the 512-byte half row (one coalesced row per instruction).
 template <typename IdxT>
-__device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q,
-                              const CUtensorMap* tm_kv, uint8_t* base, Bars* b, uint32_t rank,
-                              int lane) {
+__device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint8_t* base,
+                              Bars* b, uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
   int* rows = reinterpret_cast<int*>(base + kRowsOff);
+  const int ptid = warp * 32 + lane;
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
-  uint32_t gt = 0, qn = 0;
+  const char* kvb = reinterpret_cast<const char*>(p.kv) + 512 * rank;   // this CTA's half
+  const int c = lane;                                  // 16-byte chunk of the half row
+  const uint32_t chunk_off = (c >> 3) * 8192;          // its 64-column block
+  uint32_t gt = 0, qn = 0, q_loads = 0;
   int it = 0;
-  bool ok = true;
-  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
-    const int nv = compact_token<IdxT>(p, tok, rows, p.trace != nullptr && rank == 0, lane);
-    const int slot = it & 1;
-    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_empty[slot]),
-                                                 ((it >> 1) & 1) ^ 1, b, p.err, 1u));
-    if (!ok) break;
-    if (lane == 0) {
-      b->nvalid[slot] = nv;
-      mbar_arrive(bar_addr(b->meta_full[slot]));
+  int pending = -1;   // stage whose copies this thread issued but has not yet counted
+  for (int64_t tok = cid; tok < p.T; tok += ncl, ++it) {
+    if (ptid == 0) b->prod_stop = *reinterpret_cast<volatile int*>(&b->abort_flag);
+    named_bar_sync(1, kProducerThreads);
+    if (b->prod_stop) break;
+    if (warp == 0) {
+      const int nv = compact_token<IdxT>(p, tok, rows, p.trace != nullptr && rank == 0, lane);
+      if (lane == 0) b->prod_nv = nv;
+    }
+    named_bar_sync(1, kProducerThreads);
+    const int nv = b->prod_nv;
+    if (warp == 0) {
+      const int slot = it & 1;
+      bool ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_empty[slot]),
+                                                        ((it >> 1) & 1) ^ 1, b, p.err, 1u));
+      if (ok && lane == 0) {
+        b->nvalid[slot] = nv;
+        mbar_arrive(bar_addr(b->meta_full[slot]));
+      }
+      if (ok && nv > 0) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bar<false>(bar_addr(b->q_empty), (qn & 1) ^ 1, b, p.err, 1u));
+        if (ok && lane == 0) {
+          mbar_arrive_expect_tx(bar_addr(b->q_full), kQBytes);
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb)
+            tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 64 * cb,
+                        static_cast<int>(tok * 128), bar_addr(b->q_full));
+          ++q_loads;
+        }
+      }
     }
     if (nv == 0) continue;
-    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->q_empty), (qn & 1) ^ 1, b, p.err, 1u));
-    if (!ok) break;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(b->q_full), kQBytes);
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb)
-        tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 64 * cb,
-                    static_cast<int>(tok * 128), bar_addr(b->q_full));
-    }
     ++qn;
     const int ntiles = (nv + kTileN - 1) / kTileN;
     for (int j = 0; j < ntiles; ++j, ++gt) {
       const uint32_t s = gt % kStages, ph = (gt / kStages) & 1;
-      ok = __all_sync(0xffffffffu,
-                      wait_bar<false>(bar_addr(b->kv_empty[s]), ph ^ 1, b, p.err, 1u));
+      const bool ok = __all_sync(0xffffffffu,
+                                 wait_bar<false>(bar_addr(b->kv_empty[s]), ph ^ 1, b, p.err, 1u));
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar_addr(b->kv_full[s]), kStageBytes);
-      __syncwarp();
-      const int first = rows[j * kTileN];   // the tile's first slot is always valid
-#pragma unroll
-      for (int k = lane; k < 64; k += 32) {
-        const int g = k >> 2, cb = k & 3;   // 16 groups of 4 rows x 4 column blocks
-        const int sl = j * kTileN + g * 4;
-        const int r0 = sl + 0 < nv ? rows[sl + 0] : first;
-        const int r1 = sl + 1 < nv ? rows[sl + 1] : first;
-        const int r2 = sl + 2 < nv ? rows[sl + 2] : first;
-        const int r3 = sl + 3 < nv ? rows[sl + 3] : first;
-        tma_gather4(sbase + kKVOff + s * kStageBytes + cb * 8192 + g * 512, tm_kv,
-                    256 * int(rank) + 64 * cb, r0, r1, r2, r3, bar_addr(b->kv_full[s]));
+      const uint32_t dst = sbase + kKVOff + s * kStageBytes + chunk_off;
+#pragma unroll 8
+      for (int k = 0; k < kTileN / 2; ++k) {
+        const int r = 2 * k + warp;
+        const int sl = j * kTileN + r;
+        const bool valid = sl < nv;                    // the ragged tail is zero-filled
+        const char* src = valid ? kvb + int64_t(rows[sl]) * 1024 + c * 16 : kvb;
+        cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
       }
+      cp_async_commit();
+      if (pending >= 0) {
+        cp_async_wait<1>();
+        land_and_arrive(bar_addr(b->kv_full[pending]));
+      }
+      pending = static_cast<int>(s);
     }
-    __syncwarp();
-  }
-  // drain: every issued load must land before the CTA may exit
-  if (lane == 0) {
-    const uint32_t n = gt < kStages ? gt : kStages;
-    for (uint32_t k = 0; k < n; ++k) {
-      const uint32_t g = gt - 1 - k;
-      wait_bar<false, true>(bar_addr(b->kv_full[g % kStages]), (g / kStages) & 1, b, p.err, 1u);
+    if (pending >= 0) {
+      cp_async_wait<0>();
+      land_and_arrive(bar_addr(b->kv_full[pending]));
+      pending = -1;
     }
-    if (qn > 0) wait_bar<false, true>(bar_addr(b->q_full), (qn - 1) & 1, b, p.err, 1u);
   }
+  cp_async_wait<0>();   // drain: no copy of ours may land after the CTA exits
+  if (ptid == 0 && q_loads > 0)
+    wait_bar<false, true>(bar_addr(b->q_full), (q_loads - 1) & 1, b, p.err, 1u);
 }
 
-// Single thread (warp 1, lane 0): issues every tcgen05.mma of the CTA.
+// Warp 2, lane 0: issues every tcgen05.mma of the CTA.
 //   S(g)  = Q_half . K_half(g)^T -> S buffer g%2 (M=128, N=64, K=256: 16 MMAs)
 //   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs)
-// issued as S(0), S(1), PV(0), S(2), PV(1), ... so the next tile's scores are
-// computed while the softmax works on the current one.
+// in the order S(g+1), PV(g) -- across token boundaries as well -- so the
+// scores of the next tile are on their way while the softmax works.
 __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem) {
   const uint32_t sbase = smem_u32(base);
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTileN, false, false);
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
-  uint32_t gt = 0, qn = 0, on = 0;
+  uint32_t gt = 0, qn = 0, tokn = 0;
   int it = 0;
+  int pend_g = -1, pend_j = 0;
+  uint32_t pend_tok = 0;
 
-  auto issue_pv = [&](uint32_t g, int j) -> bool {
+  auto issue_pv = [&](uint32_t g, int j, uint32_t tk) -> bool {
     const uint32_t s = g % kStages;
     if (!wait_bar<false>(bar_addr(b->p_full), g & 1, b, p.err, 2u)) return false;
-    if (j == 0 && !wait_bar<false>(bar_addr(b->o_free), (on & 1) ^ 1, b, p.err, 2u)) return false;
+    if (j == 0 && !wait_bar<false>(bar_addr(b->o_free), (tk & 1) ^ 1, b, p.err, 2u)) return false;
     tc_fence_after();
     const uint32_t kv = sbase + kKVOff + s * kStageBytes;
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
       const uint64_t a = sdesc_sw128(sbase + kPOff + kk * 32, 16, 1024);
-      // V as MN-major B: 64-column chunks 8 KB apart, 8-slot groups 1 KB apart
+      // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart
       const uint64_t bd = sdesc_sw128(kv + kk * 16 * 128, 8192, 1024);
       mma_bf16_ss(tmem, a, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
     }
@@ -278,21 +314,35 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
       }
       mma_commit(bar_addr(b->s_full[sb]));
       if (j == ntiles - 1) mma_commit(bar_addr(b->q_empty));
-      if (j > 0 && !(ok = issue_pv(gt - 1, j - 1))) break;
+      if (pend_g >= 0 && !(ok = issue_pv(uint32_t(pend_g), pend_j, pend_tok))) break;
+      pend_g = static_cast<int>(gt);
+      pend_j = j;
+      pend_tok = tokn;
     }
-    if (!ok) break;
-    if (!(ok = issue_pv(gt - 1, ntiles - 1))) break;
     ++qn;
-    ++on;
+    ++tokn;
   }
+  if (ok && pend_g >= 0) issue_pv(uint32_t(pend_g), pend_j, pend_tok);
   // drain: every MMA issued must complete before TMEM is freed
   mma_commit(bar_addr(b->drain));
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
 }
 
-// Warps 2..5 (128 threads): thread = TMEM lane = head `row`.  Per tile: read
-// the partial S, swap it with the peer CTA, softmax, write P; per token: the
-// epilogue (sink fold, normalise, bf16 store of this CTA's half of O, lse).
+// One tile whose partial scores were sent to the peer and whose softmax is still to do.
+struct PendingTile {
+  uint32_t g;      // global tile index of this CTA
+  int j;           // tile index within its token
+  int ntiles;      // tiles of its token
+  int nv;          // valid slots of its token
+  int64_t tok;
+  uint32_t own[32];  // this CTA's partial scores of the tile, fp16x2-packed
+};
+
+// Warps 3-6 (128 threads): thread = TMEM lane = head `row`.
+//   stage A(g): read S_r(g) from TMEM, round to fp16, st.async it to the peer;
+//   stage B(g-1): combine own + peer partials, online softmax, write P, and
+//   after a token's last tile the epilogue (sink fold, normalise, bf16 store of
+//   this CTA's half of O, lse).
 __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
                              uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
@@ -300,130 +350,26 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
   const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   const uint32_t peer = rank ^ 1u;
-  const uint32_t x_mine = sbase + kXOff + row * 256;        // my row of the buffer the peer fills
-  const uint32_t x_peer = map_peer(x_mine, peer);           // my row of the peer's buffer
-  const uint32_t xfull_peer = map_peer(bar_addr(b->x_full), peer);
-  const uint32_t xfree_peer = map_peer(bar_addr(b->x_free), peer);
+  uint32_t recv_local[2], recv_peer[2], xfull_peer[2], xfree_peer[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    recv_local[i] = sbase + kXOff + i * kXBufBytes + row * 128;
+    recv_peer[i] = map_peer(recv_local[i], peer);
+    xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
+    xfree_peer[i] = map_peer(bar_addr(b->x_free[i]), peer);
+  }
   const float sl2 = p.scale * kLog2e;
   const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
   uint8_t* prow = base + kPOff + row * 128;
-  uint32_t gt = 0;
-  int it = 0;
-  bool ok = true;
+  float m_run = -INFINITY, l_run = 0.f;
+  PendingTile pend{};
+  bool has_pend = false;
 
-  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
-    const int slot = it & 1;
-    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1,
-                                                 b, p.err, 4u));
-    if (!ok) break;
-    const int nv = b->nvalid[slot];
-    mbar_arrive(bar_addr(b->meta_empty[slot]));
-    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
-                                           256 * rank);
-    if (nv == 0) {   // nothing valid: O = 0; lse = sink (finite) or -inf
-#pragma unroll
-      for (int c = 0; c < 32; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-      if (rank == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
-      continue;
-    }
-    float m_run = -INFINITY, l_run = 0.f;
-    const int ntiles = (nv + kTileN - 1) / kTileN;
-    for (int j = 0; j < ntiles; ++j, ++gt) {
-      const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
-      ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]), sph, b, p.err, 4u));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sv[64];
-      tmem_ld32(tl + kTmemS + sb * kTileN, sv);
-      tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar_addr(b->s_free[sb]));
-
-      // swap partial scores with the peer: my partial -> its buffer, its partial <- mine
-      ok = __all_sync(0xffffffffu,
-                      wait_bar<true>(bar_addr(b->x_free), (gt & 1) ^ 1, b, p.err, 4u));
-      if (!ok) break;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_cluster_v4(x_peer + ((c ^ (row & 15)) << 4), __uint_as_float(sv[4 * c]),
-                      __uint_as_float(sv[4 * c + 1]), __uint_as_float(sv[4 * c + 2]),
-                      __uint_as_float(sv[4 * c + 3]));
-      mbar_arrive_remote(xfull_peer);
-      ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full), gt & 1, b, p.err, 4u));
-      if (!ok) break;
-      float s[64];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(base + kXOff + row * 256 +
-                                                          ((c ^ (row & 15)) << 4));
-        s[4 * c + 0] = __uint_as_float(sv[4 * c + 0]) + v.x;
-        s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + v.y;
-        s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + v.z;
-        s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + v.w;
-      }
-      mbar_arrive_remote(xfree_peer);
-
-      // online softmax, base 2; columns past the valid count are -inf
-      const int nvt = min(kTileN, nv - j * kTileN);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
-        mx = fmaxf(mx, s[i]);
-      }
-      const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_run - mx);
-        m_run = mx;
-      }
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        s[i] = ex2(s[i] - m_run);
-        sum += s[i];
-      }
-      l_run = l_run * alpha + sum;
-
-      // the previous P.V must be done before P is overwritten or O rescaled
-      if (gt > 0) {
-        ok = __all_sync(0xffffffffu,
-                        wait_bar<false>(bar_addr(b->pv_done), (gt - 1) & 1, b, p.err, 4u));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + 32 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tl + 32 * c, o);
-        }
-        tmem_wait_st();
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 w;
-        w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
-        w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
-        w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
-        w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
-        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = w;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_addr(b->p_full));
-    }
-    if (!ok) break;
-
-    // epilogue: wait for the last P.V, fold the sink, normalise, store
-    ok = __all_sync(0xffffffffu,
-                    wait_bar<false>(bar_addr(b->pv_done), (gt - 1) & 1, b, p.err, 4u));
-    if (!ok) break;
+  // epilogue of token `tok` whose last tile is g_last
+  auto epilogue = [&](int64_t tok, uint32_t g_last) -> bool {
+    if (!__all_sync(0xffffffffu,
+                    wait_bar<false>(bar_addr(b->pv_done), g_last & 1, b, p.err, 4u)))
+      return false;
     tc_fence_after();
     float m2 = m_run, l2 = l_run;
     if (sk != -INFINITY) {
@@ -431,6 +377,8 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
       l2 = l_run * ex2(m_run - m2) + ex2(sk - m2);
     }
     const float f = ex2(m_run - m2) / l2;
+    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
+                                           256 * rank);
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       uint32_t o[32];
@@ -449,13 +397,161 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     tc_fence_before();
     mbar_arrive(bar_addr(b->o_free));
     if (rank == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
+    return true;
+  };
+
+  // stage B of the pending tile
+  auto finish = [&]() -> bool {
+    const uint32_t g = pend.g, xb = g & 1;
+    if (!__all_sync(0xffffffffu,
+                    wait_bar<true>(bar_addr(b->x_full[xb]), (g >> 1) & 1, b, p.err, 4u)))
+      return false;
+    float s[64];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(
+          base + (recv_local[xb] - sbase) + ((c ^ (row & 7)) << 4));
+      const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 a = unpack_f16x2(pend.own[4 * c + q]);
+        const float2 e = unpack_f16x2(pv[q]);
+        s[8 * c + 2 * q] = a.x + e.x;       // f16(own) + f16(peer): the same sum in both CTAs
+        s[8 * c + 2 * q + 1] = a.y + e.y;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote(xfree_peer[xb]);   // my buffer xb may be refilled
+    if (pend.j == 0) {
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+    // online softmax, base 2; columns past the valid count are -inf
+    const int nvt = min(kTileN, pend.nv - pend.j * kTileN);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
+      mx = fmaxf(mx, s[i]);
+    }
+    const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
+    float alpha = 1.f;
+    if (need) {
+      alpha = ex2(m_run - mx);
+      m_run = mx;
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      s[i] = ex2(s[i] - m_run);
+      sum += s[i];
+    }
+    l_run = l_run * alpha + sum;
+    // the previous P.V must be done before P is overwritten or O rescaled
+    if (g > 0) {
+      if (!__all_sync(0xffffffffu,
+                      wait_bar<false>(bar_addr(b->pv_done), (g - 1) & 1, b, p.err, 4u)))
+        return false;
+      tc_fence_after();
+    }
+    if (pend.j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tl + 32 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tl + 32 * c, o);
+      }
+      tmem_wait_st();
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 w;
+      w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
+      w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
+      w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
+      w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
+      *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = w;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar_addr(b->p_full));
+    if (pend.j == pend.ntiles - 1) return epilogue(pend.tok, g);
+    return true;
+  };
+
+  uint32_t gt = 0;
+  int it = 0;
+  bool ok = true;
+  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
+    const int slot = it & 1;
+    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1,
+                                                 b, p.err, 4u));
+    if (!ok) break;
+    const int nv = b->nvalid[slot];
+    mbar_arrive(bar_addr(b->meta_empty[slot]));
+    if (nv == 0) {   // nothing valid: O = 0; lse = sink (finite) or -inf
+      if (has_pend) {
+        has_pend = false;
+        if (!(ok = finish())) break;
+      }
+      uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
+                                             256 * rank);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (rank == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
+      continue;
+    }
+    const int ntiles = (nv + kTileN - 1) / kTileN;
+    for (int j = 0; j < ntiles; ++j, ++gt) {
+      // ---- stage A(gt): partial scores out of TMEM, fp16, to the peer
+      const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
+      if (!(ok = __all_sync(0xffffffffu,
+                            wait_bar<false>(bar_addr(b->s_full[sb]), sph, b, p.err, 4u))))
+        break;
+      tc_fence_after();
+      uint32_t own[32];
+      {
+        uint32_t sv[64];
+        tmem_ld32(tl + kTmemS + sb * kTileN, sv);
+        tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_addr(b->s_free[sb]));
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+      }
+      // the peer has consumed what I sent into its buffer sb two tiles ago
+      if (!(ok = __all_sync(0xffffffffu,
+                            wait_bar<true>(bar_addr(b->x_free[sb]), sph ^ 1, b, p.err, 4u))))
+        break;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(recv_peer[sb] + ((c ^ (row & 7)) << 4),
+                    make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
+                    xfull_peer[sb]);
+      if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[sb]), kXBufBytes);
+      // ---- stage B of the previous tile
+      if (has_pend && !(ok = finish())) break;
+      pend.g = gt;
+      pend.j = j;
+      pend.ntiles = ntiles;
+      pend.nv = nv;
+      pend.tok = tok;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pend.own[i] = own[i];
+      has_pend = true;
+    }
   }
+  if (ok && has_pend) finish();
 }
 
 template <typename IdxT>
 __global__ void __launch_bounds__(kThreads, 1)
-    h128_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_kv, const H128Params p) {
+    h128_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const H128Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* b = reinterpret_cast<Bars*>(base + kBarOff);
@@ -466,29 +562,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(b->q_full), 1);
     mbar_init(bar_addr(b->q_empty), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_addr(b->kv_full[s]), 1);
+      mbar_init(bar_addr(b->kv_full[s]), kProducerThreads);
       mbar_init(bar_addr(b->kv_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->s_full[i]), 1);
       mbar_init(bar_addr(b->s_free[i]), 128);
+      mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
+      mbar_init(bar_addr(b->x_free[i]), 4);     // one arrive per peer softmax warp
       mbar_init(bar_addr(b->meta_full[i]), 1);
       mbar_init(bar_addr(b->meta_empty[i]), 1 + 128);
     }
     mbar_init(bar_addr(b->p_full), 128);
     mbar_init(bar_addr(b->pv_done), 1);
-    mbar_init(bar_addr(b->x_full), 128);
-    mbar_init(bar_addr(b->x_free), 128);
     mbar_init(bar_addr(b->o_free), 128);
     mbar_init(bar_addr(b->drain), 1);
     b->abort_flag = 0;
+    b->prod_stop = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_kv);
-  }
-  if (warp == 1) {
+  if (warp == 0 && lane == 0) prefetch_tmap(&tm_q);
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&b->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -498,9 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();   // the peer's barriers are initialised before any remote arrive
   const uint32_t tmem = b->tmem_base;
 
-  if (warp == 0) {
-    producer_role<IdxT>(p, &tm_q, &tm_kv, base, b, rank, lane);
-  } else if (warp == 1) {
+  if (warp < 2) {
+    producer_role<IdxT>(p, &tm_q, base, b, rank, warp, lane);
+  } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role(p, base, b, tmem);
     __syncwarp();
   } else {
@@ -510,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();   // no remote store or arrive may target an exited CTA
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -552,23 +646,29 @@ struct DeviceState {
   int max_clusters = 0;
 };
 
-template <typename IdxT>
-cudaError_t prepare(DeviceState& st) {
-  auto kern = h128_fwd_kernel<IdxT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return e;
+cudaLaunchConfig_t launch_config(unsigned ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
+  cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
-  cudaLaunchAttribute attr[1];
+  cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <typename IdxT>
+cudaError_t prepare(DeviceState& st) {
+  auto kern = h128_fwd_kernel<IdxT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(2, nullptr, attr);
   int n = 0;
   e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
   if (e != cudaSuccess) return e;
@@ -601,15 +701,15 @@ cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   DeviceState* st = nullptr;
   cudaError_t e = device_state<IdxT>(&st);
   if (e != cudaSuccess) return e;
-  CUtensorMap tq, tkv;
-  if (!make_map(&tq, fp.q, static_cast<uint64_t>(fp.T) * 128, 64, 128) ||
-      !make_map(&tkv, fp.kv, static_cast<uint64_t>(fp.num_kv), 64, 1))
+  CUtensorMap tq;
+  if (!make_map(&tq, fp.q, static_cast<uint64_t>(fp.T) * 128, 64, 128))
     return cudaErrorInvalidValue;
   unsigned int* err = nullptr;
   if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_h128_error)) != cudaSuccess)
     return e;
   H128Params p;
   p.idx = fp.idx;
+  p.kv = static_cast<const __nv_bfloat16*>(fp.kv);
   p.sink = fp.sink;
   p.out = static_cast<__nv_bfloat16*>(fp.out);
   p.lse = fp.lse;
@@ -620,21 +720,10 @@ cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   p.topk = fp.topk;
   p.idx64 = fp.idx64;
   p.scale = fp.scale;
-
   const int64_t clusters = fp.T < st->max_clusters ? fp.T : st->max_clusters;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, h128_fwd_kernel<IdxT>, tq, tkv, p);
+  cudaLaunchConfig_t cfg = launch_config(static_cast<unsigned>(2 * clusters), stream, attr);
+  e = cudaLaunchKernelEx(&cfg, h128_fwd_kernel<IdxT>, tq, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
