@@ -298,6 +298,12 @@ const char* sparse_mla_strerror(int32_t status) {
 
 const char* sparse_mla_last_cuda_error(void) { return g_last_cuda_error; }
 
+#ifdef SMLA_TIMELINE
+// Debug builds only (-DSMLA_TIMELINE): copy the H=128 kernel's cluster-0 role
+// timeline (2 ranks x 4 roles x 64 tiles x 8 events of clock64) to host memory.
+int sparse_mla_debug_timeline(long long* host) { return smla::h128_timeline(host); }
+#endif
+
 int32_t sparse_mla_abi_version(void) { return kAbiVersion; }
 
 }  // extern "C"

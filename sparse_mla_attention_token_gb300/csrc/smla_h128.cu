@@ -112,6 +112,21 @@ struct H128Params {
 
 __device__ unsigned int g_h128_error;
 
+// Optional per-role timeline of cluster 0 (clock64 per event, first 64 tiles),
+// compiled only with -DSMLA_TIMELINE for performance investigations.
+#ifdef SMLA_TIMELINE
+__device__ long long g_timeline[2][4][64][8];
+#define SMLA_TL(role, g, ev)                                             \
+  do {                                                                   \
+    if (cluster_id_x() == 0 && (g) < 64)                                 \
+      g_timeline[cluster_ctarank()][role][g][ev] = clock64();            \
+  } while (0)
+#else
+#define SMLA_TL(role, g, ev) \
+  do {                       \
+  } while (0)
+#endif
+
 // Bounded mbarrier wait; false on timeout or (unless kDrain) when another role
 // gave up.  Drain waits ignore the abort flag: they wait for work already in
 // flight (copies, MMAs), bounded by time alone.
@@ -228,6 +243,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
       const bool ok = __all_sync(0xffffffffu,
                                  wait_bar<false>(bar_addr(b->kv_empty[s]), ph ^ 1, b, p.err, 1u));
       if (!ok) break;
+      if (ptid == 0) SMLA_TL(0, gt, 0);
       const uint32_t dst = sbase + kKVOff + s * kStageBytes + chunk_off;
 #pragma unroll 8
       for (int k = 0; k < kTileN / 2; ++k) {
@@ -238,9 +254,11 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
       }
       cp_async_commit();
+      if (ptid == 0) SMLA_TL(0, gt, 1);
       if (pending >= 0) {
         cp_async_wait<1>();
         land_and_arrive(bar_addr(b->kv_full[pending]));
+        if (ptid == 0) SMLA_TL(0, gt, 2);
       }
       pending = static_cast<int>(s);
     }
@@ -267,12 +285,15 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
   uint32_t gt = 0, qn = 0, tokn = 0;
   int it = 0;
-  int pend_g = -1, pend_j = 0;
-  uint32_t pend_tok = 0;
+  // P.V of a tile is issued two tiles after its S (two S buffers), so the
+  // softmax always finds the next scores computed.  pend[0] is the older.
+  int pend_g[2] = {-1, -1}, pend_j[2] = {0, 0};
+  uint32_t pend_tok[2] = {0, 0};
 
   auto issue_pv = [&](uint32_t g, int j, uint32_t tk) -> bool {
     const uint32_t s = g % kStages;
     if (!wait_bar<false>(bar_addr(b->p_full), g & 1, b, p.err, 2u)) return false;
+    SMLA_TL(1, g, 3);
     if (j == 0 && !wait_bar<false>(bar_addr(b->o_free), (tk & 1) ^ 1, b, p.err, 2u)) return false;
     tc_fence_after();
     const uint32_t kv = sbase + kKVOff + s * kStageBytes;
@@ -285,6 +306,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
     }
     mma_commit(bar_addr(b->kv_empty[s]));
     mma_commit(bar_addr(b->pv_done));
+    SMLA_TL(1, g, 4);
     return true;
   };
 
@@ -302,7 +324,9 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
       const uint32_t s = gt % kStages, ph = (gt / kStages) & 1;
       const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
       if (!(ok = wait_bar<false>(bar_addr(b->kv_full[s]), ph, b, p.err, 2u))) break;
+      SMLA_TL(1, gt, 1);
       if (!(ok = wait_bar<false>(bar_addr(b->s_free[sb]), sph ^ 1, b, p.err, 2u))) break;
+      SMLA_TL(1, gt, 2);
       tc_fence_after();
       const uint32_t kv = sbase + kKVOff + s * kStageBytes;
 #pragma unroll
@@ -313,16 +337,21 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
         mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
       }
       mma_commit(bar_addr(b->s_full[sb]));
+      SMLA_TL(1, gt, 0);
       if (j == ntiles - 1) mma_commit(bar_addr(b->q_empty));
-      if (pend_g >= 0 && !(ok = issue_pv(uint32_t(pend_g), pend_j, pend_tok))) break;
-      pend_g = static_cast<int>(gt);
-      pend_j = j;
-      pend_tok = tokn;
+      if (pend_g[0] >= 0 && !(ok = issue_pv(uint32_t(pend_g[0]), pend_j[0], pend_tok[0]))) break;
+      pend_g[0] = pend_g[1];
+      pend_j[0] = pend_j[1];
+      pend_tok[0] = pend_tok[1];
+      pend_g[1] = static_cast<int>(gt);
+      pend_j[1] = j;
+      pend_tok[1] = tokn;
     }
     ++qn;
     ++tokn;
   }
-  if (ok && pend_g >= 0) issue_pv(uint32_t(pend_g), pend_j, pend_tok);
+  for (int k = 0; k < 2 && ok; ++k)
+    if (pend_g[k] >= 0) ok = issue_pv(uint32_t(pend_g[k]), pend_j[k], pend_tok[k]);
   // drain: every MMA issued must complete before TMEM is freed
   mma_commit(bar_addr(b->drain));
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
@@ -403,9 +432,11 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
   // stage B of the pending tile
   auto finish = [&]() -> bool {
     const uint32_t g = pend.g, xb = g & 1;
+    if (row == 0) SMLA_TL(3, g, 0);
     if (!__all_sync(0xffffffffu,
                     wait_bar<true>(bar_addr(b->x_full[xb]), (g >> 1) & 1, b, p.err, 4u)))
       return false;
+    if (row == 0) SMLA_TL(3, g, 1);
     float s[64];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -447,6 +478,7 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
       sum += s[i];
     }
     l_run = l_run * alpha + sum;
+    if (row == 0) SMLA_TL(3, g, 2);
     // the previous P.V must be done before P is overwritten or O rescaled
     if (g > 0) {
       if (!__all_sync(0xffffffffu,
@@ -454,6 +486,7 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         return false;
       tc_fence_after();
     }
+    if (row == 0) SMLA_TL(3, g, 3);
     if (pend.j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -478,6 +511,7 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(bar_addr(b->p_full));
+    if (row == 0) SMLA_TL(3, g, 4);
     if (pend.j == pend.ntiles - 1) return epilogue(pend.tok, g);
     return true;
   };
@@ -508,9 +542,11 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     for (int j = 0; j < ntiles; ++j, ++gt) {
       // ---- stage A(gt): partial scores out of TMEM, fp16, to the peer
       const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
+      if (row == 0) SMLA_TL(2, gt, 0);
       if (!(ok = __all_sync(0xffffffffu,
                             wait_bar<false>(bar_addr(b->s_full[sb]), sph, b, p.err, 4u))))
         break;
+      if (row == 0) SMLA_TL(2, gt, 1);
       tc_fence_after();
       uint32_t own[32];
       {
@@ -525,15 +561,18 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
           own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
       }
       // the peer has consumed what I sent into its buffer sb two tiles ago
+      if (row == 0) SMLA_TL(2, gt, 2);
       if (!(ok = __all_sync(0xffffffffu,
                             wait_bar<true>(bar_addr(b->x_free[sb]), sph ^ 1, b, p.err, 4u))))
         break;
+      if (row == 0) SMLA_TL(2, gt, 3);
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         st_async_v4(recv_peer[sb] + ((c ^ (row & 7)) << 4),
                     make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
                     xfull_peer[sb]);
       if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[sb]), kXBufBytes);
+      if (row == 0) SMLA_TL(2, gt, 4);
       // ---- stage B of the previous tile
       if (has_pend && !(ok = finish())) break;
       pend.g = gt;
@@ -752,6 +791,12 @@ int h128_geometry(int64_t T, LaunchGeom* g) {
   g->smem = static_cast<int>(kSmemBytes);
   return 0;
 }
+
+#ifdef SMLA_TIMELINE
+int h128_timeline(long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_timeline, sizeof(g_timeline)));
+}
+#endif
 
 int h128_error_word(unsigned int** addr) {
   return static_cast<int>(cudaGetSymbolAddress(reinterpret_cast<void**>(addr), g_h128_error));

@@ -41,6 +41,9 @@ int launch_h128(const FwdParams& p, void* stream);
 // Whether launch_h128 supports this problem (H == 128, 1 <= topk <= 2048,
 // num_kv >= 1, T < 2^24).
 bool h128_supported(int64_t T, int32_t H, int32_t topk, int64_t num_kv);
+#ifdef SMLA_TIMELINE
+int h128_timeline(long long* host);
+#endif
 // Device address of the h128 kernel's error word (bounded waits), or nullptr.
 int h128_error_word(unsigned int** addr);
 
