@@ -19,10 +19,10 @@
 // Data movement.  Producer warp 0 compacts the token's valid slots
 // (0 <= idx < num_kv at the index's full width; PR #6002 "Invalid KV rows",
 // "int64 indices") into a row list and loads the token's Q half with 2-D TMA.
-// Producer warps 0 and 1 gather 64 half rows (512 B each) per tile with
-// 16-byte cp.async straight into the 128-byte-swizzled layout of a 3-stage
-// ring; each thread fences its landed copies into the async proxy before it
-// arrives on the stage's barrier.  One tile serves as the K-major B operand of
+// Producer warps 0-2, one per stage of a 3-stage ring, gather 64 half rows
+// (512 B each) per tile with 16-byte cp.async straight into the
+// 128-byte-swizzled layout; each fences its landed copies into the async
+// proxy before it arrives on its stage's barrier.  One tile serves as the K-major B operand of
 // Q.K^T and the MN-major B operand of P.V.  The ragged tail of a token's last
 // tile is zero-filled and its scores are masked: no invalid slot is read.
 //
@@ -33,8 +33,8 @@
 // the running max is only raised when it grows by more than 2^8, which keeps
 // O rescales rare and is exact because O and l use the same stale max.
 //
-// Warps (224 threads): 0-1 producers, 2 TMEM owner + single-thread MMA issuer,
-// 3-6 softmax + epilogue (thread = TMEM lane = head).  Every mbarrier wait is
+// Warps (256 threads): 0-2 producers, 3 TMEM owner + single-thread MMA issuer,
+// 4-7 softmax + epilogue (thread = TMEM lane = head).  Every mbarrier wait is
 // bounded: on expiry the kernel sets an error word, every role leaves its
 // loop, in-flight copies and MMAs are drained, TMEM is freed and the kernel
 // returns.
@@ -54,12 +54,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 224;
-constexpr int kProducerThreads = 64;  // warps 0-1
-constexpr int kMmaWarp = 2;
+constexpr int kThreads = 256;
+constexpr int kProducerThreads = 96;  // warps 0-2, one per KV stage
+constexpr int kMmaWarp = 3;
 constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 3;
-constexpr int kMaxTopk = 2048;        // row-list capacity
+constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;      // S buffers start at this column (O at 0)
 
@@ -73,7 +73,7 @@ constexpr uint32_t kPBytes = 128 * kTileN * 2;        // 16 KB
 constexpr uint32_t kXOff = kPOff + kPBytes;           // peer partials: [2][128 rows][64 fp16]
 constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
 constexpr uint32_t kRowsOff = kXOff + 2 * kXBufBytes; // int32 row list
-constexpr uint32_t kBarOff = kRowsOff + kMaxTopk * 4;
+constexpr uint32_t kBarOff = kRowsOff + 2 * kMaxTopk * 4;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024; // + barriers + alignment slack
 
 constexpr long long kTimeoutCycles = 4000000000LL;    // ~2 s at 2 GHz
@@ -88,7 +88,7 @@ struct Bars {
   uint64_t meta_full[2], meta_empty[2];
   uint64_t drain;
   int nvalid[2];
-  int prod_nv;
+  int prod_nv[2];
   int prod_stop;
   uint32_t tmem_base;
   int abort_flag;
@@ -188,32 +188,37 @@ __device__ __forceinline__ void land_and_arrive(uint32_t bar) {
   mbar_arrive(bar);
 }
 
-// Warps 0-1.  Warp 0 compacts the index list and loads Q (2-D TMA); both warps
-// gather the tile's half rows: warp w copies rows w, w+2, ..., lane c copies
-// 16-byte chunk c of the 512-byte half row (one coalesced row per instruction).
+// Warps 0-2.  Warp s owns KV stage s: it copies every tile g with g % 3 == s
+// (64 half rows of 512 B; lane c copies 16-byte chunk c of every row, so each
+// instruction moves one contiguous half row) and, once its own copies have
+// landed, fences them into the async proxy and arrives on the stage's
+// barrier.  A tile's readiness therefore depends only on its stage being
+// free.  Warp 0 also compacts the index lists one token ahead into a
+// double-buffered row list, publishes each token's valid count and loads the
+// token's Q half with 2-D TMA.
 template <typename IdxT>
 __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint8_t* base,
                               Bars* b, uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
-  int* rows = reinterpret_cast<int*>(base + kRowsOff);
-  const int ptid = warp * 32 + lane;
+  int* rows_buf = reinterpret_cast<int*>(base + kRowsOff);   // [2][kMaxTopk]
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   const char* kvb = reinterpret_cast<const char*>(p.kv) + 512 * rank;   // this CTA's half
   const int c = lane;                                  // 16-byte chunk of the half row
   const uint32_t chunk_off = (c >> 3) * 8192;          // its 64-column block
+  const bool trace = p.trace != nullptr && rank == 0;
   uint32_t gt = 0, qn = 0, q_loads = 0;
   int it = 0;
-  int pending = -1;   // stage whose copies this thread issued but has not yet counted
+  if (warp == 0 && cid < p.T) {
+    const int nv = compact_token<IdxT>(p, cid, rows_buf, trace, lane);
+    if (lane == 0) b->prod_nv[0] = nv;
+  }
   for (int64_t tok = cid; tok < p.T; tok += ncl, ++it) {
-    if (ptid == 0) b->prod_stop = *reinterpret_cast<volatile int*>(&b->abort_flag);
-    named_bar_sync(1, kProducerThreads);
+    const int buf = it & 1;
+    if (warp == 0 && lane == 0) b->prod_stop = *reinterpret_cast<volatile int*>(&b->abort_flag);
+    named_bar_sync(1, kProducerThreads);   // this token's list is complete; token it-1 is done
     if (b->prod_stop) break;
-    if (warp == 0) {
-      const int nv = compact_token<IdxT>(p, tok, rows, p.trace != nullptr && rank == 0, lane);
-      if (lane == 0) b->prod_nv = nv;
-    }
-    named_bar_sync(1, kProducerThreads);
-    const int nv = b->prod_nv;
+    const int nv = b->prod_nv[buf];
+    const int* rows = rows_buf + buf * kMaxTopk;
     if (warp == 0) {
       const int slot = it & 1;
       bool ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_empty[slot]),
@@ -235,45 +240,49 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         }
       }
     }
-    if (nv == 0) continue;
-    ++qn;
-    const int ntiles = (nv + kTileN - 1) / kTileN;
-    for (int j = 0; j < ntiles; ++j, ++gt) {
-      const uint32_t s = gt % kStages, ph = (gt / kStages) & 1;
-      const bool ok = __all_sync(0xffffffffu,
-                                 wait_bar<false>(bar_addr(b->kv_empty[s]), ph ^ 1, b, p.err, 1u));
-      if (!ok) break;
-      if (ptid == 0) SMLA_TL(0, gt, 0);
-      const uint32_t dst = sbase + kKVOff + s * kStageBytes + chunk_off;
+    const int64_t next = tok + ncl;
+    bool compacted = (warp != 0) || (next >= p.T);
+    auto compact_next = [&]() {
+      const int nn = compact_token<IdxT>(p, next, rows_buf + (buf ^ 1) * kMaxTopk, trace, lane);
+      if (lane == 0) b->prod_nv[buf ^ 1] = nn;
+      compacted = true;
+    };
+    if (nv > 0) {
+      ++qn;
+      const int ntiles = (nv + kTileN - 1) / kTileN;
+      for (int j = 0; j < ntiles; ++j) {
+        const uint32_t g = gt + j;
+        if (static_cast<int>(g % kStages) != warp) continue;
+        const uint32_t ph = (g / kStages) & 1;
+        const bool ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->kv_empty[warp]),
+                                                                ph ^ 1, b, p.err, 1u));
+        if (!ok) break;
+        SMLA_TL(0, g, 0);
+        const uint32_t dst = sbase + kKVOff + warp * kStageBytes + chunk_off;
 #pragma unroll 8
-      for (int k = 0; k < kTileN / 2; ++k) {
-        const int r = 2 * k + warp;
-        const int sl = j * kTileN + r;
-        const bool valid = sl < nv;                    // the ragged tail is zero-filled
-        const char* src = valid ? kvb + int64_t(rows[sl]) * 1024 + c * 16 : kvb;
-        cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        for (int r = 0; r < kTileN; ++r) {
+          const int sl = j * kTileN + r;
+          const bool valid = sl < nv;                  // the ragged tail is zero-filled
+          const char* src = valid ? kvb + int64_t(rows[sl]) * 1024 + c * 16 : kvb;
+          cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        }
+        cp_async_commit();
+        SMLA_TL(0, g, 1);
+        if (!compacted && j + kStages >= ntiles) compact_next();   // overlaps the copies
+        cp_async_wait<0>();
+        land_and_arrive(bar_addr(b->kv_full[warp]));
+        SMLA_TL(0, g, 2);
       }
-      cp_async_commit();
-      if (ptid == 0) SMLA_TL(0, gt, 1);
-      if (pending >= 0) {
-        cp_async_wait<1>();
-        land_and_arrive(bar_addr(b->kv_full[pending]));
-        if (ptid == 0) SMLA_TL(0, gt, 2);
-      }
-      pending = static_cast<int>(s);
+      gt += ntiles;
     }
-    if (pending >= 0) {
-      cp_async_wait<0>();
-      land_and_arrive(bar_addr(b->kv_full[pending]));
-      pending = -1;
-    }
+    if (!compacted) compact_next();
   }
   cp_async_wait<0>();   // drain: no copy of ours may land after the CTA exits
-  if (ptid == 0 && q_loads > 0)
+  if (warp == 0 && lane == 0 && q_loads > 0)
     wait_bar<false, true>(bar_addr(b->q_full), (q_loads - 1) & 1, b, p.err, 1u);
 }
 
-// Warp 2, lane 0: issues every tcgen05.mma of the CTA.
+// Warp 3, lane 0: issues every tcgen05.mma of the CTA.
 //   S(g)  = Q_half . K_half(g)^T -> S buffer g%2 (M=128, N=64, K=256: 16 MMAs)
 //   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs)
 // in the order S(g+1), PV(g) -- across token boundaries as well -- so the
@@ -367,7 +376,7 @@ struct PendingTile {
   uint32_t own[32];  // this CTA's partial scores of the tile, fp16x2-packed
 };
 
-// Warps 3-6 (128 threads): thread = TMEM lane = head `row`.
+// Warps 4-7 (128 threads): thread = TMEM lane = head `row`.
 //   stage A(g): read S_r(g) from TMEM, round to fp16, st.async it to the peer;
 //   stage B(g-1): combine own + peer partials, online softmax, write P, and
 //   after a token's last tile the epilogue (sink fold, normalise, bf16 store of
@@ -601,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(b->q_full), 1);
     mbar_init(bar_addr(b->q_empty), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_addr(b->kv_full[s]), kProducerThreads);
+      mbar_init(bar_addr(b->kv_full[s]), 32);     // the stage's producer warp
       mbar_init(bar_addr(b->kv_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -631,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();   // the peer's barriers are initialised before any remote arrive
   const uint32_t tmem = b->tmem_base;
 
-  if (warp < 2) {
+  if (warp < kMmaWarp) {
     producer_role<IdxT>(p, &tm_q, base, b, rank, warp, lane);
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role(p, base, b, tmem);

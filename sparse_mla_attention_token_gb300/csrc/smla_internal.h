@@ -38,7 +38,7 @@ int launch_smallh(const FwdParams& p, void* stream);
 
 // tcgen05 kernel for H == 128, splits == 1.
 int launch_h128(const FwdParams& p, void* stream);
-// Whether launch_h128 supports this problem (H == 128, 1 <= topk <= 2048,
+// Whether launch_h128 supports this problem (H == 128, 1 <= topk <= 1024,
 // num_kv >= 1, T < 2^24).
 bool h128_supported(int64_t T, int32_t H, int32_t topk, int64_t num_kv);
 #ifdef SMLA_TIMELINE
