@@ -462,30 +462,41 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     }
     __syncwarp();
     if (lane == 0) mbar_arrive_remote(xfree_peer[xb]);   // my buffer xb may be refilled
+    if (row == 0) SMLA_TL(3, g, 5);
     if (pend.j == 0) {
       m_run = -INFINITY;
       l_run = 0.f;
     }
-    // online softmax, base 2; columns past the valid count are -inf
+    // online softmax, base 2; columns past the valid count are -inf.  The
+    // reductions run as 8 independent partial chains (no 64-long dependency).
     const int nvt = min(kTileN, pend.nv - pend.j * kTileN);
-    float mx = -INFINITY;
+    float mx8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
       s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
-      mx = fmaxf(mx, s[i]);
+      mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
     }
+    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+    if (row == 0) SMLA_TL(3, g, 6);
     const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
     float alpha = 1.f;
     if (need) {
       alpha = ex2(m_run - mx);
       m_run = mx;
     }
-    float sum = 0.f;
+    float sum8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
       s[i] = ex2(s[i] - m_run);
-      sum += s[i];
+      sum8[i & 7] += s[i];
     }
+    const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                      ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
     l_run = l_run * alpha + sum;
     if (row == 0) SMLA_TL(3, g, 2);
     // the previous P.V must be done before P is overwritten or O rescaled
