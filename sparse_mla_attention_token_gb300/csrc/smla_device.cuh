@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 namespace smla {
@@ -62,11 +63,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 // Packed fp16x2 -> the two floats (exact).
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
-  float lo, hi;
-  asm("{\n.reg .f16 l, h;\nmov.b32 {l, h}, %2;\ncvt.f32.f16 %0, l;\ncvt.f32.f16 %1, h;\n}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(v));
-  return make_float2(lo, hi);
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
 // The hardware base-2 exponential (MUFU.EX2): ex2.approx.ftz.f32.

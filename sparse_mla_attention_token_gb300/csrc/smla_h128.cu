@@ -259,11 +259,16 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         if (!ok) break;
         SMLA_TL(0, g, 0);
         const uint32_t dst = sbase + kKVOff + warp * kStageBytes + chunk_off;
-#pragma unroll 8
+        // the tile's 64 row indices, two per lane, broadcast by shuffle below
+        // (a shared-memory load per row would serialise behind each copy)
+        const int ra = j * kTileN + lane, rb = ra + 32;
+        const int row_a = ra < nv ? rows[ra] : -1;
+        const int row_b = rb < nv ? rows[rb] : -1;
+#pragma unroll
         for (int r = 0; r < kTileN; ++r) {
-          const int sl = j * kTileN + r;
-          const bool valid = sl < nv;                  // the ragged tail is zero-filled
-          const char* src = valid ? kvb + int64_t(rows[sl]) * 1024 + c * 16 : kvb;
+          const int rr = __shfl_sync(0xffffffffu, r < 32 ? row_a : row_b, r & 31);
+          const bool valid = rr >= 0;                  // the ragged tail is zero-filled
+          const char* src = valid ? kvb + int64_t(rr) * 1024 + c * 16 : kvb;
           cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
         }
         cp_async_commit();
@@ -460,8 +465,6 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         s[8 * c + 2 * q + 1] = a.y + e.y;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive_remote(xfree_peer[xb]);   // my buffer xb may be refilled
     if (row == 0) SMLA_TL(3, g, 5);
     if (pend.j == 0) {
       m_run = -INFINITY;
@@ -480,6 +483,11 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     }
     const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                            fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+    // Buffer xb may be refilled: every lane's reads of it have returned (the
+    // row max above consumed all of them) before lane 0 signals, and the
+    // peer writes it again only two tiles later.
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
     if (row == 0) SMLA_TL(3, g, 6);
     const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
     float alpha = 1.f;
