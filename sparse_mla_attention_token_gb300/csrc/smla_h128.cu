@@ -19,10 +19,10 @@
 // Data movement.  Producer warp 0 compacts the token's valid slots
 // (0 <= idx < num_kv at the index's full width; PR #6002 "Invalid KV rows",
 // "int64 indices") into a row list and loads the token's Q half with 2-D TMA.
-// Producer warps 0-2, one per stage of a 3-stage ring, gather 64 half rows
-// (512 B each) per tile with 16-byte cp.async straight into the
-// 128-byte-swizzled layout; each fences its landed copies into the async
-// proxy before it arrives on its stage's barrier.  One tile serves as the K-major B operand of
+// Producer warps 0-2 gather each tile's 64 half rows (512 B each) with
+// 16-byte cp.async straight into the 128-byte-swizzled layout of a 3-stage
+// ring; each fences its landed copies into the async proxy before it arrives
+// on the stage's barrier.  One tile serves as the K-major B operand of
 // Q.K^T and the MN-major B operand of P.V.  The ragged tail of a token's last
 // tile is zero-filled and its scores are masked: no invalid slot is read.
 //
@@ -33,8 +33,9 @@
 // the running max is only raised when it grows by more than 2^8, which keeps
 // O rescales rare and is exact because O and l use the same stale max.
 //
-// Warps (256 threads): 0-2 producers, 3 TMEM owner + single-thread MMA issuer,
-// 4-7 softmax + epilogue (thread = TMEM lane = head).  Every mbarrier wait is
+// Warps (384 threads): 0-2 producers, 3 TMEM owner + single-thread MMA issuer,
+// 4-11 softmax + epilogue: two threads per head (TMEM lane), each owning half
+// of the tile's 64 score columns and half of the row's 256 O columns.  Every mbarrier wait is
 // bounded: on expiry the kernel sets an error word, every role leaves its
 // loop, in-flight copies and MMAs are drained, TMEM is freed and the kernel
 // returns.
@@ -54,9 +55,10 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 256;
-constexpr int kProducerThreads = 96;  // warps 0-2, one per KV stage
+constexpr int kThreads = 384;
+constexpr int kProducerThreads = 96;  // warps 0-2
 constexpr int kMmaWarp = 3;
+constexpr int kSoftmaxThreads = 256;  // warps 4-11: two threads per head row
 constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 3;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
@@ -74,7 +76,9 @@ constexpr uint32_t kXOff = kPOff + kPBytes;           // peer partials: [2][128 
 constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
 constexpr uint32_t kRowsOff = kXOff + 2 * kXBufBytes; // int32 row list
 constexpr uint32_t kBarOff = kRowsOff + 2 * kMaxTopk * 4;
-constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024; // + barriers + alignment slack
+constexpr uint32_t kExOff = kBarOff + 256;            // row max / row sum exchange (fp32)
+constexpr uint32_t kExBytes = (2 * 2 * 128 + 2 * 128) * 4;
+constexpr uint32_t kSmemBytes = kExOff + kExBytes + 1024;   // + alignment slack
 
 constexpr long long kTimeoutCycles = 4000000000LL;    // ~2 s at 2 GHz
 
@@ -87,6 +91,8 @@ struct Bars {
   uint64_t o_free;
   uint64_t meta_full[2], meta_empty[2];
   uint64_t drain;
+  uint64_t rmax_bar[2];   // both halves of every row posted their partial max
+  uint64_t lsum_bar;      // both halves posted their partial sum (epilogue)
   int nvalid[2];
   int prod_nv[2];
   int prod_stop;
@@ -188,14 +194,14 @@ __device__ __forceinline__ void land_and_arrive(uint32_t bar) {
   mbar_arrive(bar);
 }
 
-// Warps 0-2.  Warp s owns KV stage s: it copies every tile g with g % 3 == s
-// (64 half rows of 512 B; lane c copies 16-byte chunk c of every row, so each
-// instruction moves one contiguous half row) and, once its own copies have
-// landed, fences them into the async proxy and arrives on the stage's
-// barrier.  A tile's readiness therefore depends only on its stage being
-// free.  Warp 0 also compacts the index lists one token ahead into a
-// double-buffered row list, publishes each token's valid count and loads the
-// token's Q half with 2-D TMA.
+// Warps 0-2 gather every tile together: warp w copies rows w, w+3, ... (lane c
+// copies 16-byte chunk c of each 512-byte half row, one contiguous half row
+// per instruction).  Each warp counts its copies on the stage's barrier once
+// they have landed and been fenced into the async proxy, overlapping them with
+// the next tile's issue only when that tile's stage is already free.  Warp 0
+// also compacts the index lists one token ahead into a double-buffered row
+// list, publishes each token's valid count and loads the token's Q half with
+// 2-D TMA.
 template <typename IdxT>
 __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint8_t* base,
                               Bars* b, uint32_t rank, int warp, int lane) {
@@ -250,33 +256,50 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
     if (nv > 0) {
       ++qn;
       const int ntiles = (nv + kTileN - 1) / kTileN;
+      int pending = -1;   // stage whose copies this warp issued but has not counted yet
       for (int j = 0; j < ntiles; ++j) {
         const uint32_t g = gt + j;
-        if (static_cast<int>(g % kStages) != warp) continue;
-        const uint32_t ph = (g / kStages) & 1;
-        const bool ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->kv_empty[warp]),
+        const uint32_t s = g % kStages, ph = (g / kStages) & 1;
+        // Overlap the previous tile's copies with this issue only if this
+        // stage is already free; otherwise count them first, so a tile's
+        // readiness never waits on a later stage.
+        if (pending >= 0 &&
+            !__all_sync(0xffffffffu, mbar_test_wait(bar_addr(b->kv_empty[s]), ph ^ 1))) {
+          cp_async_wait<0>();
+          land_and_arrive(bar_addr(b->kv_full[pending]));
+          pending = -1;
+        }
+        const bool ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->kv_empty[s]),
                                                                 ph ^ 1, b, p.err, 1u));
         if (!ok) break;
         SMLA_TL(0, g, 0);
-        const uint32_t dst = sbase + kKVOff + warp * kStageBytes + chunk_off;
-        // the tile's 64 row indices, two per lane, broadcast by shuffle below
-        // (a shared-memory load per row would serialise behind each copy)
-        const int ra = j * kTileN + lane, rb = ra + 32;
-        const int row_a = ra < nv ? rows[ra] : -1;
-        const int row_b = rb < nv ? rows[rb] : -1;
+        const uint32_t dst = sbase + kKVOff + s * kStageBytes + chunk_off;
+        // this warp copies rows r = warp + 3k; lane k holds row k's index
+        const int rk = warp + 3 * lane, sl = j * kTileN + rk;
+        const int my_row = (rk < kTileN && sl < nv) ? rows[sl] : -1;
 #pragma unroll
-        for (int r = 0; r < kTileN; ++r) {
-          const int rr = __shfl_sync(0xffffffffu, r < 32 ? row_a : row_b, r & 31);
-          const bool valid = rr >= 0;                  // the ragged tail is zero-filled
-          const char* src = valid ? kvb + int64_t(rr) * 1024 + c * 16 : kvb;
-          cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        for (int k = 0; k < 22; ++k) {
+          const int r = warp + 3 * k;
+          const int rr = __shfl_sync(0xffffffffu, my_row, k);
+          if (r < kTileN) {
+            const bool valid = rr >= 0;                // the ragged tail is zero-filled
+            const char* src = valid ? kvb + int64_t(rr) * 1024 + c * 16 : kvb;
+            cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+          }
         }
         cp_async_commit();
         SMLA_TL(0, g, 1);
-        if (!compacted && j + kStages >= ntiles) compact_next();   // overlaps the copies
+        if (!compacted && j == ntiles - 1) compact_next();   // overlaps the copies
+        if (pending >= 0) {
+          cp_async_wait<1>();
+          land_and_arrive(bar_addr(b->kv_full[pending]));
+        }
+        pending = static_cast<int>(s);
+      }
+      if (pending >= 0) {
         cp_async_wait<0>();
-        land_and_arrive(bar_addr(b->kv_full[warp]));
-        SMLA_TL(0, g, 2);
+        land_and_arrive(bar_addr(b->kv_full[pending]));
+        SMLA_TL(0, gt + ntiles - 1, 2);
       }
       gt += ntiles;
     }
@@ -378,18 +401,23 @@ struct PendingTile {
   int ntiles;      // tiles of its token
   int nv;          // valid slots of its token
   int64_t tok;
-  uint32_t own[32];  // this CTA's partial scores of the tile, fp16x2-packed
+  uint32_t own[16];  // this thread's 32 partial scores of the tile, fp16x2-packed
 };
 
-// Warps 4-7 (128 threads): thread = TMEM lane = head `row`.
-//   stage A(g): read S_r(g) from TMEM, round to fp16, st.async it to the peer;
-//   stage B(g-1): combine own + peer partials, online softmax, write P, and
-//   after a token's last tile the epilogue (sink fold, normalise, bf16 store of
-//   this CTA's half of O, lse).
+// Warps 4-11 (256 threads).  Thread (row, half): row = TMEM lane = head, half
+// = which 32 of the tile's 64 score columns and which 128 of the row's 256 O
+// columns it owns (warps 4-7: half 0, warps 8-11: half 1).
+//   stage A(g): read its S_r(g) columns from TMEM, round to fp16, st.async
+//     them to the peer;
+//   stage B(g-1): combine own + peer partials, row max across both halves
+//     (shared memory + an mbarrier), online softmax, write its P columns, and
+//     after a token's last tile the epilogue (row sum across both halves, sink
+//     fold, normalise, bf16 store of its O columns, lse).
 __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
                              uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
   const int row = 32 * (warp & 3) + lane;
+  const int half = (warp - 4) >> 2;
   const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   const uint32_t peer = rank ^ 1u;
@@ -401,31 +429,41 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
     xfree_peer[i] = map_peer(bar_addr(b->x_free[i]), peer);
   }
+  float* rmax = reinterpret_cast<float*>(base + kExOff);          // [2 parity][2 half][128]
+  float* lsum = rmax + 2 * 2 * 128;                               // [2 half][128]
   const float sl2 = p.scale * kLog2e;
   const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
   uint8_t* prow = base + kPOff + row * 128;
   float m_run = -INFINITY, l_run = 0.f;
+  uint32_t epi_n = 0;   // epilogues done (phase of lsum_bar)
   PendingTile pend{};
   bool has_pend = false;
 
   // epilogue of token `tok` whose last tile is g_last
   auto epilogue = [&](int64_t tok, uint32_t g_last) -> bool {
+    lsum[half * 128 + row] = l_run;
+    mbar_arrive(bar_addr(b->lsum_bar));
+    if (!__all_sync(0xffffffffu,
+                    wait_bar<false>(bar_addr(b->lsum_bar), epi_n & 1, b, p.err, 4u)))
+      return false;
+    ++epi_n;
+    const float lt = lsum[row] + lsum[128 + row];   // same order in both halves
     if (!__all_sync(0xffffffffu,
                     wait_bar<false>(bar_addr(b->pv_done), g_last & 1, b, p.err, 4u)))
       return false;
     tc_fence_after();
-    float m2 = m_run, l2 = l_run;
+    float m2 = m_run, l2 = lt;
     if (sk != -INFINITY) {
       m2 = fmaxf(m_run, sk);
-      l2 = l_run * ex2(m_run - m2) + ex2(sk - m2);
+      l2 = lt * ex2(m_run - m2) + ex2(sk - m2);
     }
     const float f = ex2(m_run - m2) / l2;
     uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
-                                           256 * rank);
+                                           256 * rank + 128 * half);
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
-      tmem_ld32(tl + 32 * c, o);
+      tmem_ld32(tl + 128 * half + 32 * c, o);
       tmem_wait_ld();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -439,23 +477,24 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     }
     tc_fence_before();
     mbar_arrive(bar_addr(b->o_free));
-    if (rank == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
+    if (rank == 0 && half == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
     return true;
   };
 
   // stage B of the pending tile
   auto finish = [&]() -> bool {
     const uint32_t g = pend.g, xb = g & 1;
-    if (row == 0) SMLA_TL(3, g, 0);
+    if (row == 0 && half == 0) SMLA_TL(3, g, 0);
     if (!__all_sync(0xffffffffu,
                     wait_bar<true>(bar_addr(b->x_full[xb]), (g >> 1) & 1, b, p.err, 4u)))
       return false;
-    if (row == 0) SMLA_TL(3, g, 1);
-    float s[64];
+    if (row == 0 && half == 0) SMLA_TL(3, g, 1);
+    float s[32];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
+      const int cc = 4 * half + c;
       const uint4 v = *reinterpret_cast<const uint4*>(
-          base + (recv_local[xb] - sbase) + ((c ^ (row & 7)) << 4));
+          base + (recv_local[xb] - sbase) + ((cc ^ (row & 7)) << 4));
       const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -465,48 +504,50 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         s[8 * c + 2 * q + 1] = a.y + e.y;
       }
     }
-    if (row == 0) SMLA_TL(3, g, 5);
     if (pend.j == 0) {
       m_run = -INFINITY;
       l_run = 0.f;
     }
-    // online softmax, base 2; columns past the valid count are -inf.  The
-    // reductions run as 8 independent partial chains (no 64-long dependency).
-    const int nvt = min(kTileN, pend.nv - pend.j * kTileN);
-    float mx8[8];
+    // online softmax, base 2; columns past the valid count are -inf
+    const int nvt = min(kTileN, pend.nv - pend.j * kTileN) - 32 * half;
+    float mx4[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+    for (int k = 0; k < 4; ++k) mx4[k] = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
+    for (int i = 0; i < 32; ++i) {
       s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
-      mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+      mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
     }
-    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+    const float mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     // Buffer xb may be refilled: every lane's reads of it have returned (the
     // row max above consumed all of them) before lane 0 signals, and the
     // peer writes it again only two tiles later.
     __syncwarp();
     if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
-    if (row == 0) SMLA_TL(3, g, 6);
+    // the row max over both halves
+    rmax[(xb * 2 + half) * 128 + row] = mh;
+    mbar_arrive(bar_addr(b->rmax_bar[xb]));
+    if (!__all_sync(0xffffffffu,
+                    wait_bar<false>(bar_addr(b->rmax_bar[xb]), (g >> 1) & 1, b, p.err, 4u)))
+      return false;
+    const float mx = fmaxf(rmax[xb * 256 + row], rmax[xb * 256 + 128 + row]);
+    if (row == 0 && half == 0) SMLA_TL(3, g, 6);
     const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
     float alpha = 1.f;
     if (need) {
       alpha = ex2(m_run - mx);
       m_run = mx;
     }
-    float sum8[8];
+    float sum4[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
+    for (int k = 0; k < 4; ++k) sum4[k] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
+    for (int i = 0; i < 32; ++i) {
       s[i] = ex2(s[i] - m_run);
-      sum8[i & 7] += s[i];
+      sum4[i & 3] += s[i];
     }
-    const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                      ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-    l_run = l_run * alpha + sum;
-    if (row == 0) SMLA_TL(3, g, 2);
+    l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+    if (row == 0 && half == 0) SMLA_TL(3, g, 2);
     // the previous P.V must be done before P is overwritten or O rescaled
     if (g > 0) {
       if (!__all_sync(0xffffffffu,
@@ -514,32 +555,32 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         return false;
       tc_fence_after();
     }
-    if (row == 0) SMLA_TL(3, g, 3);
+    if (row == 0 && half == 0) SMLA_TL(3, g, 3);
     if (pend.j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 32 * c, o);
+        tmem_ld32(tl + 128 * half + 32 * c, o);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tl + 32 * c, o);
+        tmem_st32(tl + 128 * half + 32 * c, o);
       }
       tmem_wait_st();
     }
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       uint4 w;
       w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
       w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
       w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
       w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
-      *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = w;
+      *reinterpret_cast<uint4*>(prow + (((4 * half + c) ^ (row & 7)) << 4)) = w;
     }
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(bar_addr(b->p_full));
-    if (row == 0) SMLA_TL(3, g, 4);
+    if (row == 0 && half == 0) SMLA_TL(3, g, 4);
     if (pend.j == pend.ntiles - 1) return epilogue(pend.tok, g);
     return true;
   };
@@ -560,47 +601,49 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         if (!(ok = finish())) break;
       }
       uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
-                                             256 * rank);
+                                             256 * rank + 128 * half);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-      if (rank == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
+      for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (rank == 0 && half == 0)
+        p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
       continue;
     }
     const int ntiles = (nv + kTileN - 1) / kTileN;
     for (int j = 0; j < ntiles; ++j, ++gt) {
-      // ---- stage A(gt): partial scores out of TMEM, fp16, to the peer
+      // ---- stage A(gt): this thread's partial scores out of TMEM, fp16, to the peer
       const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
-      if (row == 0) SMLA_TL(2, gt, 0);
+      if (row == 0 && half == 0) SMLA_TL(2, gt, 0);
       if (!(ok = __all_sync(0xffffffffu,
                             wait_bar<false>(bar_addr(b->s_full[sb]), sph, b, p.err, 4u))))
         break;
-      if (row == 0) SMLA_TL(2, gt, 1);
+      if (row == 0 && half == 0) SMLA_TL(2, gt, 1);
       tc_fence_after();
-      uint32_t own[32];
+      uint32_t own[16];
       {
-        uint32_t sv[64];
-        tmem_ld32(tl + kTmemS + sb * kTileN, sv);
-        tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
+        uint32_t sv[32];
+        tmem_ld32(tl + kTmemS + sb * kTileN + 32 * half, sv);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar_addr(b->s_free[sb]));
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
           own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
       }
+      if (row == 0 && half == 0) SMLA_TL(2, gt, 2);
       // the peer has consumed what I sent into its buffer sb two tiles ago
-      if (row == 0) SMLA_TL(2, gt, 2);
       if (!(ok = __all_sync(0xffffffffu,
                             wait_bar<true>(bar_addr(b->x_free[sb]), sph ^ 1, b, p.err, 4u))))
         break;
-      if (row == 0) SMLA_TL(2, gt, 3);
+      if (row == 0 && half == 0) SMLA_TL(2, gt, 3);
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(recv_peer[sb] + ((c ^ (row & 7)) << 4),
+      for (int c = 0; c < 4; ++c) {
+        const int cc = 4 * half + c;
+        st_async_v4(recv_peer[sb] + ((cc ^ (row & 7)) << 4),
                     make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
                     xfull_peer[sb]);
-      if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[sb]), kXBufBytes);
-      if (row == 0) SMLA_TL(2, gt, 4);
+      }
+      if (row == 0 && half == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[sb]), kXBufBytes);
+      if (row == 0 && half == 0) SMLA_TL(2, gt, 4);
       // ---- stage B of the previous tile
       if (has_pend && !(ok = finish())) break;
       pend.g = gt;
@@ -609,7 +652,7 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
       pend.nv = nv;
       pend.tok = tok;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pend.own[i] = own[i];
+      for (int i = 0; i < 16; ++i) pend.own[i] = own[i];
       has_pend = true;
     }
   }
@@ -629,20 +672,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(b->q_full), 1);
     mbar_init(bar_addr(b->q_empty), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_addr(b->kv_full[s]), 32);     // the stage's producer warp
+      mbar_init(bar_addr(b->kv_full[s]), kProducerThreads);
       mbar_init(bar_addr(b->kv_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->s_full[i]), 1);
-      mbar_init(bar_addr(b->s_free[i]), 128);
+      mbar_init(bar_addr(b->s_free[i]), kSoftmaxThreads);
       mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
-      mbar_init(bar_addr(b->x_free[i]), 4);     // one arrive per peer softmax warp
+      mbar_init(bar_addr(b->x_free[i]), 8);     // one arrive per peer softmax warp
+      mbar_init(bar_addr(b->rmax_bar[i]), kSoftmaxThreads);
       mbar_init(bar_addr(b->meta_full[i]), 1);
-      mbar_init(bar_addr(b->meta_empty[i]), 1 + 128);
+      mbar_init(bar_addr(b->meta_empty[i]), 1 + kSoftmaxThreads);
     }
-    mbar_init(bar_addr(b->p_full), 128);
+    mbar_init(bar_addr(b->p_full), kSoftmaxThreads);
     mbar_init(bar_addr(b->pv_done), 1);
-    mbar_init(bar_addr(b->o_free), 128);
+    mbar_init(bar_addr(b->o_free), kSoftmaxThreads);
+    mbar_init(bar_addr(b->lsum_bar), kSoftmaxThreads);
     mbar_init(bar_addr(b->drain), 1);
     b->abort_flag = 0;
     b->prod_stop = 0;
