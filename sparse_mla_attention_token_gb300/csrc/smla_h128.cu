@@ -243,6 +243,12 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
             tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 64 * cb,
                         static_cast<int>(tok * 128), bar_addr(b->q_full));
           ++q_loads;
+          // the next token's Q half into L2 now, so its load at the token switch is short
+          if (tok + ncl < p.T) {
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb)
+              tma_prefetch_2d(tm_q, 256 * int(rank) + 64 * cb, static_cast<int>((tok + ncl) * 128));
+          }
         }
       }
     }
