@@ -63,20 +63,20 @@ constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 3;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 256;      // S buffers start at this column (O at 0)
+constexpr uint32_t kTmemS = 256;      // two S buffers (64 columns each)
+constexpr uint32_t kTmemP = 384;      // two P buffers (32 columns of bf16 pairs each); O at 0
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kQOff = 0;                         // [4 col blocks][128 rows][128 B]
 constexpr uint32_t kQBytes = 128 * 256 * 2;           // 64 KB
 constexpr uint32_t kKVOff = kQOff + kQBytes;          // [stage][4 col blocks][64 rows][128 B]
 constexpr uint32_t kStageBytes = kTileN * 256 * 2;    // 32 KB
-constexpr uint32_t kPOff = kKVOff + kStages * kStageBytes;   // [128 rows][128 B] bf16
-constexpr uint32_t kPBytes = 128 * kTileN * 2;        // 16 KB
-constexpr uint32_t kXOff = kPOff + kPBytes;           // peer partials: [2][128 rows][64 fp16]
+constexpr uint32_t kXOff = kKVOff + kStages * kStageBytes;   // peer partials: [3][128][64 fp16]
+constexpr int kXBufs = 3;
 constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
-constexpr uint32_t kRowsOff = kXOff + 2 * kXBufBytes; // int32 row list
+constexpr uint32_t kRowsOff = kXOff + kXBufs * kXBufBytes;   // int32 row lists
 constexpr uint32_t kBarOff = kRowsOff + 2 * kMaxTopk * 4;
-constexpr uint32_t kExOff = kBarOff + 256;            // row max / row sum exchange (fp32)
+constexpr uint32_t kExOff = kBarOff + 512;            // row max / row sum exchange (fp32)
 constexpr uint32_t kExBytes = (2 * 2 * 128 + 2 * 128) * 4;
 constexpr uint32_t kSmemBytes = kExOff + kExBytes + 1024;   // + alignment slack
 
@@ -86,8 +86,8 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done;
-  uint64_t x_full[2], x_free[2];
+  uint64_t p_full[2], pv_done[2];   // per P buffer
+  uint64_t x_full[kXBufs], x_free[kXBufs];
   uint64_t o_free;
   uint64_t meta_full[2], meta_empty[2];
   uint64_t drain;
@@ -99,7 +99,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 struct H128Params {
   const void* idx;
@@ -318,7 +318,8 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
 
 // Warp 3, lane 0: issues every tcgen05.mma of the CTA.
 //   S(g)  = Q_half . K_half(g)^T -> S buffer g%2 (M=128, N=64, K=256: 16 MMAs)
-//   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs)
+//   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs,
+//           P(g) read from TMEM buffer g%2, V from the shared-memory stage)
 // in the order S(g+1), PV(g) -- across token boundaries as well -- so the
 // scores of the next tile are on their way while the softmax works.
 __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem) {
@@ -335,20 +336,20 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
 
   auto issue_pv = [&](uint32_t g, int j, uint32_t tk) -> bool {
     const uint32_t s = g % kStages;
-    if (!wait_bar<false>(bar_addr(b->p_full), g & 1, b, p.err, 2u)) return false;
+    if (!wait_bar<false>(bar_addr(b->p_full[g & 1]), (g >> 1) & 1, b, p.err, 2u)) return false;
     SMLA_TL(1, g, 3);
     if (j == 0 && !wait_bar<false>(bar_addr(b->o_free), (tk & 1) ^ 1, b, p.err, 2u)) return false;
     tc_fence_after();
     const uint32_t kv = sbase + kKVOff + s * kStageBytes;
+    const uint32_t ptm = tmem + kTmemP + (g & 1) * 32;   // P(g) in TMEM: 64 bf16 = 32 columns
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
-      const uint64_t a = sdesc_sw128(sbase + kPOff + kk * 32, 16, 1024);
       // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart
       const uint64_t bd = sdesc_sw128(kv + kk * 16 * 128, 8192, 1024);
-      mma_bf16_ss(tmem, a, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_bf16_ts(tmem, ptm + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
     }
     mma_commit(bar_addr(b->kv_empty[s]));
-    mma_commit(bar_addr(b->pv_done));
+    mma_commit(bar_addr(b->pv_done[g & 1]));
     SMLA_TL(1, g, 4);
     return true;
   };
@@ -427,9 +428,11 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
   const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   const uint32_t peer = rank ^ 1u;
-  uint32_t recv_local[2], recv_peer[2], xfull_peer[2], xfree_peer[2];
+  // Three receive buffers: tile g goes to buffer g%3; the peer refills it
+  // (tile g+3) after I signal that my reads of tile g are done.
+  uint32_t recv_local[kXBufs], recv_peer[kXBufs], xfull_peer[kXBufs], xfree_peer[kXBufs];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kXBufs; ++i) {
     recv_local[i] = sbase + kXOff + i * kXBufBytes + row * 128;
     recv_peer[i] = map_peer(recv_local[i], peer);
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
@@ -439,7 +442,6 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
   float* lsum = rmax + 2 * 2 * 128;                               // [2 half][128]
   const float sl2 = p.scale * kLog2e;
   const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
-  uint8_t* prow = base + kPOff + row * 128;
   float m_run = -INFINITY, l_run = 0.f;
   uint32_t epi_n = 0;   // epilogues done (phase of lsum_bar)
   PendingTile pend{};
@@ -454,8 +456,8 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
       return false;
     ++epi_n;
     const float lt = lsum[row] + lsum[128 + row];   // same order in both halves
-    if (!__all_sync(0xffffffffu,
-                    wait_bar<false>(bar_addr(b->pv_done), g_last & 1, b, p.err, 4u)))
+    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[g_last & 1]),
+                                                 (g_last >> 1) & 1, b, p.err, 4u)))
       return false;
     tc_fence_after();
     float m2 = m_run, l2 = lt;
@@ -489,10 +491,10 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
 
   // stage B of the pending tile
   auto finish = [&]() -> bool {
-    const uint32_t g = pend.g, xb = g & 1;
+    const uint32_t g = pend.g, xb = g % kXBufs, pb = g & 1;
     if (row == 0 && half == 0) SMLA_TL(3, g, 0);
-    if (!__all_sync(0xffffffffu,
-                    wait_bar<true>(bar_addr(b->x_full[xb]), (g >> 1) & 1, b, p.err, 4u)))
+    if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]), (g / kXBufs) & 1, b,
+                                                p.err, 4u)))
       return false;
     if (row == 0 && half == 0) SMLA_TL(3, g, 1);
     float s[32];
@@ -526,17 +528,16 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     }
     const float mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     // Buffer xb may be refilled: every lane's reads of it have returned (the
-    // row max above consumed all of them) before lane 0 signals, and the
-    // peer writes it again only two tiles later.
+    // row max above consumed all of them) before lane 0 signals.
     __syncwarp();
     if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
     // the row max over both halves
-    rmax[(xb * 2 + half) * 128 + row] = mh;
-    mbar_arrive(bar_addr(b->rmax_bar[xb]));
+    rmax[(pb * 2 + half) * 128 + row] = mh;
+    mbar_arrive(bar_addr(b->rmax_bar[pb]));
     if (!__all_sync(0xffffffffu,
-                    wait_bar<false>(bar_addr(b->rmax_bar[xb]), (g >> 1) & 1, b, p.err, 4u)))
+                    wait_bar<false>(bar_addr(b->rmax_bar[pb]), (g >> 1) & 1, b, p.err, 4u)))
       return false;
-    const float mx = fmaxf(rmax[xb * 256 + row], rmax[xb * 256 + 128 + row]);
+    const float mx = fmaxf(rmax[pb * 256 + row], rmax[pb * 256 + 128 + row]);
     if (row == 0 && half == 0) SMLA_TL(3, g, 6);
     const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
     float alpha = 1.f;
@@ -554,15 +555,19 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     }
     l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
     if (row == 0 && half == 0) SMLA_TL(3, g, 2);
-    // the previous P.V must be done before P is overwritten or O rescaled
-    if (g > 0) {
-      if (!__all_sync(0xffffffffu,
-                      wait_bar<false>(bar_addr(b->pv_done), (g - 1) & 1, b, p.err, 4u)))
+    // P buffer pb was last read by P.V(g-2); O may only be rescaled after P.V(g-1)
+    if (g >= 2) {
+      if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb]),
+                                                   ((g >> 1) & 1) ^ 1, b, p.err, 4u)))
         return false;
       tc_fence_after();
     }
     if (row == 0 && half == 0) SMLA_TL(3, g, 3);
     if (pend.j > 0 && __any_sync(0xffffffffu, need)) {
+      if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb ^ 1]),
+                                                   ((g - 1) >> 1) & 1, b, p.err, 4u)))
+        return false;
+      tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -572,20 +577,14 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
         tmem_st32(tl + 128 * half + 32 * c, o);
       }
-      tmem_wait_st();
     }
+    uint32_t pk[16];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4 w;
-      w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
-      w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
-      w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
-      w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
-      *reinterpret_cast<uint4*>(prow + (((4 * half + c) ^ (row & 7)) << 4)) = w;
-    }
-    fence_proxy_async_smem();
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+    tmem_st16(tl + kTmemP + pb * 32 + 16 * half, pk);
+    tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(bar_addr(b->p_full));
+    mbar_arrive(bar_addr(b->p_full[pb]));
     if (row == 0 && half == 0) SMLA_TL(3, g, 4);
     if (pend.j == pend.ntiles - 1) return epilogue(pend.tok, g);
     return true;
@@ -636,19 +635,20 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
           own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
       }
       if (row == 0 && half == 0) SMLA_TL(2, gt, 2);
-      // the peer has consumed what I sent into its buffer sb two tiles ago
-      if (!(ok = __all_sync(0xffffffffu,
-                            wait_bar<true>(bar_addr(b->x_free[sb]), sph ^ 1, b, p.err, 4u))))
+      const uint32_t xb = gt % kXBufs;
+      // the peer has consumed what I sent into its buffer xb three tiles ago
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_free[xb]),
+                                                        ((gt / kXBufs) & 1) ^ 1, b, p.err, 4u))))
         break;
       if (row == 0 && half == 0) SMLA_TL(2, gt, 3);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int cc = 4 * half + c;
-        st_async_v4(recv_peer[sb] + ((cc ^ (row & 7)) << 4),
+        st_async_v4(recv_peer[xb] + ((cc ^ (row & 7)) << 4),
                     make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
-                    xfull_peer[sb]);
+                    xfull_peer[xb]);
       }
-      if (row == 0 && half == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[sb]), kXBufBytes);
+      if (row == 0 && half == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
       if (row == 0 && half == 0) SMLA_TL(2, gt, 4);
       // ---- stage B of the previous tile
       if (has_pend && !(ok = finish())) break;
@@ -684,14 +684,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->s_full[i]), 1);
       mbar_init(bar_addr(b->s_free[i]), kSoftmaxThreads);
-      mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
-      mbar_init(bar_addr(b->x_free[i]), 8);     // one arrive per peer softmax warp
+      mbar_init(bar_addr(b->p_full[i]), kSoftmaxThreads);
+      mbar_init(bar_addr(b->pv_done[i]), 1);
       mbar_init(bar_addr(b->rmax_bar[i]), kSoftmaxThreads);
       mbar_init(bar_addr(b->meta_full[i]), 1);
       mbar_init(bar_addr(b->meta_empty[i]), 1 + kSoftmaxThreads);
     }
-    mbar_init(bar_addr(b->p_full), kSoftmaxThreads);
-    mbar_init(bar_addr(b->pv_done), 1);
+    for (int i = 0; i < kXBufs; ++i) {
+      mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
+      mbar_init(bar_addr(b->x_free[i]), 8);     // one arrive per peer softmax warp
+    }
     mbar_init(bar_addr(b->o_free), kSoftmaxThreads);
     mbar_init(bar_addr(b->lsum_bar), kSoftmaxThreads);
     mbar_init(bar_addr(b->drain), 1);
