@@ -34,8 +34,8 @@
 // O rescales rare and is exact because O and l use the same stale max.
 //
 // Warps (384 threads): 0-2 producers, 3 TMEM owner + single-thread MMA issuer,
-// 4-11 softmax + epilogue: two threads per head (TMEM lane), each owning half
-// of the tile's 64 score columns and half of the row's 256 O columns.  Every mbarrier wait is
+// 4-7 score swap with the peer CTA, 8-11 softmax + epilogue (thread = TMEM
+// lane = head in both warpgroups).  Every mbarrier wait is
 // bounded: on expiry the kernel sets an error word, every role leaves its
 // loop, in-flight copies and MMAs are drained, TMEM is freed and the kernel
 // returns.
@@ -58,13 +58,15 @@ using namespace sm100;
 constexpr int kThreads = 384;
 constexpr int kProducerThreads = 96;  // warps 0-2
 constexpr int kMmaWarp = 3;
-constexpr int kSoftmaxThreads = 256;  // warps 4-11: two threads per head row
+constexpr int kSwapThreads = 128;     // warps 4-7: one thread per head row
+constexpr int kSoftmaxThreads = 128;  // warps 8-11: one thread per head row
 constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 3;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 256;      // two S buffers (64 columns each)
-constexpr uint32_t kTmemP = 384;      // two P buffers (32 columns of bf16 pairs each); O at 0
+constexpr int kSBufs = 3;
+constexpr uint32_t kTmemS = 256;      // three S buffers (64 columns each)
+constexpr uint32_t kTmemP = 448;      // two P buffers (32 columns of bf16 pairs each); O at 0
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kQOff = 0;                         // [4 col blocks][128 rows][128 B]
@@ -76,23 +78,21 @@ constexpr int kXBufs = 3;
 constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
 constexpr uint32_t kRowsOff = kXOff + kXBufs * kXBufBytes;   // int32 row lists
 constexpr uint32_t kBarOff = kRowsOff + 2 * kMaxTopk * 4;
-constexpr uint32_t kExOff = kBarOff + 512;            // row max / row sum exchange (fp32)
-constexpr uint32_t kExBytes = (2 * 2 * 128 + 2 * 128) * 4;
-constexpr uint32_t kSmemBytes = kExOff + kExBytes + 1024;   // + alignment slack
+constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
 
 constexpr long long kTimeoutCycles = 4000000000LL;    // ~2 s at 2 GHz
 
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], s_free[2];
+  uint64_t s_full[kSBufs];   // partial S(g) in TMEM (MMA commit)
+  uint64_t s_comb[kSBufs];   // full S(g) written back by the swap warpgroup
+  uint64_t s_free[kSBufs];   // the softmax has read S(g)
   uint64_t p_full[2], pv_done[2];   // per P buffer
   uint64_t x_full[kXBufs], x_free[kXBufs];
   uint64_t o_free;
   uint64_t meta_full[2], meta_empty[2];
   uint64_t drain;
-  uint64_t rmax_bar[2];   // both halves of every row posted their partial max
-  uint64_t lsum_bar;      // both halves posted their partial sum (epilogue)
   int nvalid[2];
   int prod_nv[2];
   int prod_stop;
@@ -317,7 +317,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
 }
 
 // Warp 3, lane 0: issues every tcgen05.mma of the CTA.
-//   S(g)  = Q_half . K_half(g)^T -> S buffer g%2 (M=128, N=64, K=256: 16 MMAs)
+//   S(g)  = Q_half . K_half(g)^T -> S buffer g%3 (M=128, N=64, K=256: 16 MMAs)
 //   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs,
 //           P(g) read from TMEM buffer g%2, V from the shared-memory stage)
 // in the order S(g+1), PV(g) -- across token boundaries as well -- so the
@@ -329,8 +329,8 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
   uint32_t gt = 0, qn = 0, tokn = 0;
   int it = 0;
-  // P.V of a tile is issued two tiles after its S (two S buffers), so the
-  // softmax always finds the next scores computed.  pend[0] is the older.
+  // P.V of a tile is issued two tiles after its S, so the swap and softmax
+  // warpgroups always find the next scores computed.  pend[0] is the older.
   int pend_g[2] = {-1, -1}, pend_j[2] = {0, 0};
   uint32_t pend_tok[2] = {0, 0};
 
@@ -366,7 +366,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
     const int ntiles = (nv + kTileN - 1) / kTileN;
     for (int j = 0; j < ntiles && ok; ++j, ++gt) {
       const uint32_t s = gt % kStages, ph = (gt / kStages) & 1;
-      const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
+      const uint32_t sb = gt % kSBufs, sph = (gt / kSBufs) & 1;
       if (!(ok = wait_bar<false>(bar_addr(b->kv_full[s]), ph, b, p.err, 2u))) break;
       SMLA_TL(1, gt, 1);
       if (!(ok = wait_bar<false>(bar_addr(b->s_free[sb]), sph ^ 1, b, p.err, 2u))) break;
@@ -401,35 +401,21 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
 }
 
-// One tile whose partial scores were sent to the peer and whose softmax is still to do.
-struct PendingTile {
-  uint32_t g;      // global tile index of this CTA
-  int j;           // tile index within its token
-  int ntiles;      // tiles of its token
-  int nv;          // valid slots of its token
-  int64_t tok;
-  uint32_t own[16];  // this thread's 32 partial scores of the tile, fp16x2-packed
-};
-
-// Warps 4-11 (256 threads).  Thread (row, half): row = TMEM lane = head, half
-// = which 32 of the tile's 64 score columns and which 128 of the row's 256 O
-// columns it owns (warps 4-7: half 0, warps 8-11: half 1).
-//   stage A(g): read its S_r(g) columns from TMEM, round to fp16, st.async
-//     them to the peer;
-//   stage B(g-1): combine own + peer partials, row max across both halves
-//     (shared memory + an mbarrier), online softmax, write its P columns, and
-//     after a token's last tile the epilogue (row sum across both halves, sink
-//     fold, normalise, bf16 store of its O columns, lse).
-__device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
-                             uint32_t rank, int warp, int lane) {
+// Warps 4-7 (128 threads), thread = TMEM lane = head `row`.  For every tile:
+//   stage 1(g): read this CTA's partial scores S_r(g) (64 fp32) from TMEM
+//     buffer g%3, round them to fp16 and st.async them into the peer's
+//     receive buffer g%3 (the bytes are counted on the peer's mbarrier);
+//   stage 2(g-1), one tile later so the swap is in flight meanwhile: add the
+//     peer's fp16 partials to its own, f16(S_0) + f16(S_1) in fp32 (the same
+//     value in both CTAs), write the full scores back into S buffer (g-1)%3 and
+//     hand them to the softmax warpgroup.
+__device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
+                          uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
   const int row = 32 * (warp & 3) + lane;
-  const int half = (warp - 4) >> 2;
   const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   const uint32_t peer = rank ^ 1u;
-  // Three receive buffers: tile g goes to buffer g%3; the peer refills it
-  // (tile g+3) after I signal that my reads of tile g are done.
   uint32_t recv_local[kXBufs], recv_peer[kXBufs], xfull_peer[kXBufs], xfree_peer[kXBufs];
 #pragma unroll
   for (int i = 0; i < kXBufs; ++i) {
@@ -438,40 +424,220 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
     xfree_peer[i] = map_peer(bar_addr(b->x_free[i]), peer);
   }
-  float* rmax = reinterpret_cast<float*>(base + kExOff);          // [2 parity][2 half][128]
-  float* lsum = rmax + 2 * 2 * 128;                               // [2 half][128]
-  const float sl2 = p.scale * kLog2e;
-  const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
-  float m_run = -INFINITY, l_run = 0.f;
-  uint32_t epi_n = 0;   // epilogues done (phase of lsum_bar)
-  PendingTile pend{};
+  uint32_t pend_own[32];
+  uint32_t pend_g = 0;
   bool has_pend = false;
 
-  // epilogue of token `tok` whose last tile is g_last
-  auto epilogue = [&](int64_t tok, uint32_t g_last) -> bool {
-    lsum[half * 128 + row] = l_run;
-    mbar_arrive(bar_addr(b->lsum_bar));
-    if (!__all_sync(0xffffffffu,
-                    wait_bar<false>(bar_addr(b->lsum_bar), epi_n & 1, b, p.err, 4u)))
+  // stage 2 of the pending tile
+  auto combine = [&]() -> bool {
+    const uint32_t g = pend_g, xb = g % kXBufs, sb = g % kSBufs;
+    if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]), (g / kXBufs) & 1, b,
+                                                p.err, 8u)))
       return false;
-    ++epi_n;
-    const float lt = lsum[row] + lsum[128 + row];   // same order in both halves
-    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[g_last & 1]),
-                                                 (g_last >> 1) & 1, b, p.err, 4u)))
-      return false;
+    uint32_t sfull[64];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(base + (recv_local[xb] - sbase) +
+                                                      ((c ^ (row & 7)) << 4));
+      const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 a = unpack_f16x2(pend_own[4 * c + q]);
+        const float2 e = unpack_f16x2(pv[q]);
+        sfull[8 * c + 2 * q] = __float_as_uint(a.x + e.x);
+        sfull[8 * c + 2 * q + 1] = __float_as_uint(a.y + e.y);
+      }
+    }
+    // buffer xb may be refilled: every lane's reads of it have been consumed above
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
+    tmem_st32(tl + kTmemS + sb * kTileN, sfull);
+    tmem_st32(tl + kTmemS + sb * kTileN + 32, sfull + 32);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar_addr(b->s_comb[sb]));
+    if (row == 0) SMLA_TL(3, g, 1);
+    return true;
+  };
+
+  uint32_t gt = 0;
+  int it = 0;
+  bool ok = true;
+  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
+    const int slot = it & 1;
+    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1,
+                                                 b, p.err, 8u));
+    if (!ok) break;
+    const int nv = b->nvalid[slot];
+    mbar_arrive(bar_addr(b->meta_empty[slot]));
+    const int ntiles = (nv + kTileN - 1) / kTileN;
+    for (int j = 0; j < ntiles; ++j, ++gt) {
+      const uint32_t sb = gt % kSBufs, xb = gt % kXBufs;
+      if (row == 0) SMLA_TL(2, gt, 0);
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]),
+                                                         (gt / kSBufs) & 1, b, p.err, 8u))))
+        break;
+      tc_fence_after();
+      uint32_t own[32];
+      {
+        uint32_t sv[64];
+        tmem_ld32(tl + kTmemS + sb * kTileN, sv);
+        tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+      }
+      if (row == 0) SMLA_TL(2, gt, 1);
+      // the peer has consumed what I sent into its buffer xb three tiles ago
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_free[xb]),
+                                                        ((gt / kXBufs) & 1) ^ 1, b, p.err, 8u))))
+        break;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(recv_peer[xb] + ((c ^ (row & 7)) << 4),
+                    make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
+                    xfull_peer[xb]);
+      if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
+      if (row == 0) SMLA_TL(2, gt, 2);
+      if (has_pend && !(ok = combine())) break;
+      pend_g = gt;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pend_own[i] = own[i];
+      has_pend = true;
+    }
+  }
+  if (ok && has_pend) combine();
+}
+
+// Warps 8-11 (128 threads), thread = TMEM lane = head `row`.  Per tile: the
+// full scores from TMEM, base-2 online softmax, P (bf16) into TMEM; after a
+// token's last tile the epilogue (sink fold, normalise, bf16 store of this
+// CTA's half of O, lse).
+__device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
+                             uint32_t rank, int warp, int lane) {
+  const int row = 32 * (warp & 3) + lane;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
+  const int64_t cid = cluster_id_x(), ncl = nclusters_x();
+  const float sl2 = p.scale * kLog2e;
+  const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
+  (void)base;
+
+  uint32_t gt = 0;
+  int it = 0;
+  bool ok = true;
+  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
+    const int slot = it & 1;
+    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1,
+                                                 b, p.err, 4u));
+    if (!ok) break;
+    const int nv = b->nvalid[slot];
+    mbar_arrive(bar_addr(b->meta_empty[slot]));
+    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
+                                           256 * rank);
+    if (nv == 0) {   // nothing valid: O = 0; lse = sink (finite) or -inf
+#pragma unroll
+      for (int c = 0; c < 32; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (rank == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
+      continue;
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    const int ntiles = (nv + kTileN - 1) / kTileN;
+    for (int j = 0; j < ntiles; ++j, ++gt) {
+      const uint32_t g = gt, sb = g % kSBufs, pb = g & 1;
+      if (row == 0) SMLA_TL(3, g, 2);
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_comb[sb]),
+                                                         (g / kSBufs) & 1, b, p.err, 4u))))
+        break;
+      if (row == 0) SMLA_TL(3, g, 3);
+      tc_fence_after();
+      float s[64];
+      {
+        uint32_t sv[64];
+        tmem_ld32(tl + kTmemS + sb * kTileN, sv);
+        tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_addr(b->s_free[sb]));
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sv[i]);
+      }
+      // online softmax, base 2; columns past the valid count are -inf
+      const int nvt = min(kTileN, nv - j * kTileN);
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
+        mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m_run - mx);
+        m_run = mx;
+      }
+      float sum8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        s[i] = ex2(s[i] - m_run);
+        sum8[i & 7] += s[i];
+      }
+      l_run = l_run * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+      // P buffer pb was last read by P.V(g-2); O may only be rescaled after P.V(g-1)
+      if (g >= 2) {
+        if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb]),
+                                                           ((g >> 1) & 1) ^ 1, b, p.err, 4u))))
+          break;
+        tc_fence_after();
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb ^ 1]),
+                                                           ((g - 1) >> 1) & 1, b, p.err, 4u))))
+          break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tl + 32 * c, o);
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+      tmem_st32(tl + kTmemP + pb * 32, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(b->p_full[pb]));
+      if (row == 0) SMLA_TL(3, g, 4);
+    }
+    if (!ok) break;
+    // epilogue: wait for the token's last P.V, fold the sink, normalise, store
+    const uint32_t gl = gt - 1;
+    if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[gl & 1]),
+                                                       (gl >> 1) & 1, b, p.err, 4u))))
+      break;
     tc_fence_after();
-    float m2 = m_run, l2 = lt;
+    float m2 = m_run, l2 = l_run;
     if (sk != -INFINITY) {
       m2 = fmaxf(m_run, sk);
-      l2 = lt * ex2(m_run - m2) + ex2(sk - m2);
+      l2 = l_run * ex2(m_run - m2) + ex2(sk - m2);
     }
     const float f = ex2(m_run - m2) / l2;
-    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
-                                           256 * rank + 128 * half);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
       uint32_t o[32];
-      tmem_ld32(tl + 128 * half + 32 * c, o);
+      tmem_ld32(tl + 32 * c, o);
       tmem_wait_ld();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -485,184 +651,8 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     }
     tc_fence_before();
     mbar_arrive(bar_addr(b->o_free));
-    if (rank == 0 && half == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
-    return true;
-  };
-
-  // stage B of the pending tile
-  auto finish = [&]() -> bool {
-    const uint32_t g = pend.g, xb = g % kXBufs, pb = g & 1;
-    if (row == 0 && half == 0) SMLA_TL(3, g, 0);
-    if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]), (g / kXBufs) & 1, b,
-                                                p.err, 4u)))
-      return false;
-    if (row == 0 && half == 0) SMLA_TL(3, g, 1);
-    float s[32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int cc = 4 * half + c;
-      const uint4 v = *reinterpret_cast<const uint4*>(
-          base + (recv_local[xb] - sbase) + ((cc ^ (row & 7)) << 4));
-      const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 a = unpack_f16x2(pend.own[4 * c + q]);
-        const float2 e = unpack_f16x2(pv[q]);
-        s[8 * c + 2 * q] = a.x + e.x;       // f16(own) + f16(peer): the same sum in both CTAs
-        s[8 * c + 2 * q + 1] = a.y + e.y;
-      }
-    }
-    if (pend.j == 0) {
-      m_run = -INFINITY;
-      l_run = 0.f;
-    }
-    // online softmax, base 2; columns past the valid count are -inf
-    const int nvt = min(kTileN, pend.nv - pend.j * kTileN) - 32 * half;
-    float mx4[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mx4[k] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
-      mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
-    }
-    const float mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-    // Buffer xb may be refilled: every lane's reads of it have returned (the
-    // row max above consumed all of them) before lane 0 signals.
-    __syncwarp();
-    if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
-    // the row max over both halves
-    rmax[(pb * 2 + half) * 128 + row] = mh;
-    mbar_arrive(bar_addr(b->rmax_bar[pb]));
-    if (!__all_sync(0xffffffffu,
-                    wait_bar<false>(bar_addr(b->rmax_bar[pb]), (g >> 1) & 1, b, p.err, 4u)))
-      return false;
-    const float mx = fmaxf(rmax[pb * 256 + row], rmax[pb * 256 + 128 + row]);
-    if (row == 0 && half == 0) SMLA_TL(3, g, 6);
-    const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
-    float alpha = 1.f;
-    if (need) {
-      alpha = ex2(m_run - mx);
-      m_run = mx;
-    }
-    float sum4[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) sum4[k] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      s[i] = ex2(s[i] - m_run);
-      sum4[i & 3] += s[i];
-    }
-    l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-    if (row == 0 && half == 0) SMLA_TL(3, g, 2);
-    // P buffer pb was last read by P.V(g-2); O may only be rescaled after P.V(g-1)
-    if (g >= 2) {
-      if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb]),
-                                                   ((g >> 1) & 1) ^ 1, b, p.err, 4u)))
-        return false;
-      tc_fence_after();
-    }
-    if (row == 0 && half == 0) SMLA_TL(3, g, 3);
-    if (pend.j > 0 && __any_sync(0xffffffffu, need)) {
-      if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb ^ 1]),
-                                                   ((g - 1) >> 1) & 1, b, p.err, 4u)))
-        return false;
-      tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tl + 128 * half + 32 * c, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tl + 128 * half + 32 * c, o);
-      }
-    }
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-    tmem_st16(tl + kTmemP + pb * 32 + 16 * half, pk);
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(bar_addr(b->p_full[pb]));
-    if (row == 0 && half == 0) SMLA_TL(3, g, 4);
-    if (pend.j == pend.ntiles - 1) return epilogue(pend.tok, g);
-    return true;
-  };
-
-  uint32_t gt = 0;
-  int it = 0;
-  bool ok = true;
-  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
-    const int slot = it & 1;
-    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1,
-                                                 b, p.err, 4u));
-    if (!ok) break;
-    const int nv = b->nvalid[slot];
-    mbar_arrive(bar_addr(b->meta_empty[slot]));
-    if (nv == 0) {   // nothing valid: O = 0; lse = sink (finite) or -inf
-      if (has_pend) {
-        has_pend = false;
-        if (!(ok = finish())) break;
-      }
-      uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
-                                             256 * rank + 128 * half);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-      if (rank == 0 && half == 0)
-        p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
-      continue;
-    }
-    const int ntiles = (nv + kTileN - 1) / kTileN;
-    for (int j = 0; j < ntiles; ++j, ++gt) {
-      // ---- stage A(gt): this thread's partial scores out of TMEM, fp16, to the peer
-      const uint32_t sb = gt & 1, sph = (gt >> 1) & 1;
-      if (row == 0 && half == 0) SMLA_TL(2, gt, 0);
-      if (!(ok = __all_sync(0xffffffffu,
-                            wait_bar<false>(bar_addr(b->s_full[sb]), sph, b, p.err, 4u))))
-        break;
-      if (row == 0 && half == 0) SMLA_TL(2, gt, 1);
-      tc_fence_after();
-      uint32_t own[16];
-      {
-        uint32_t sv[32];
-        tmem_ld32(tl + kTmemS + sb * kTileN + 32 * half, sv);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar_addr(b->s_free[sb]));
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
-      }
-      if (row == 0 && half == 0) SMLA_TL(2, gt, 2);
-      const uint32_t xb = gt % kXBufs;
-      // the peer has consumed what I sent into its buffer xb three tiles ago
-      if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_free[xb]),
-                                                        ((gt / kXBufs) & 1) ^ 1, b, p.err, 4u))))
-        break;
-      if (row == 0 && half == 0) SMLA_TL(2, gt, 3);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int cc = 4 * half + c;
-        st_async_v4(recv_peer[xb] + ((cc ^ (row & 7)) << 4),
-                    make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
-                    xfull_peer[xb]);
-      }
-      if (row == 0 && half == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
-      if (row == 0 && half == 0) SMLA_TL(2, gt, 4);
-      // ---- stage B of the previous tile
-      if (has_pend && !(ok = finish())) break;
-      pend.g = gt;
-      pend.j = j;
-      pend.ntiles = ntiles;
-      pend.nv = nv;
-      pend.tok = tok;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) pend.own[i] = own[i];
-      has_pend = true;
-    }
+    if (rank == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
   }
-  if (ok && has_pend) finish();
 }
 
 template <typename IdxT>
@@ -681,21 +671,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_addr(b->kv_full[s]), kProducerThreads);
       mbar_init(bar_addr(b->kv_empty[s]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(bar_addr(b->s_full[i]), 1);
+      mbar_init(bar_addr(b->s_comb[i]), kSwapThreads);
       mbar_init(bar_addr(b->s_free[i]), kSoftmaxThreads);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->p_full[i]), kSoftmaxThreads);
       mbar_init(bar_addr(b->pv_done[i]), 1);
-      mbar_init(bar_addr(b->rmax_bar[i]), kSoftmaxThreads);
       mbar_init(bar_addr(b->meta_full[i]), 1);
-      mbar_init(bar_addr(b->meta_empty[i]), 1 + kSoftmaxThreads);
+      mbar_init(bar_addr(b->meta_empty[i]), 1 + kSwapThreads + kSoftmaxThreads);
     }
     for (int i = 0; i < kXBufs; ++i) {
       mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
-      mbar_init(bar_addr(b->x_free[i]), 8);     // one arrive per peer softmax warp
+      mbar_init(bar_addr(b->x_free[i]), 4);     // one arrive per peer swap warp
     }
     mbar_init(bar_addr(b->o_free), kSoftmaxThreads);
-    mbar_init(bar_addr(b->lsum_bar), kSoftmaxThreads);
     mbar_init(bar_addr(b->drain), 1);
     b->abort_flag = 0;
     b->prod_stop = 0;
@@ -717,6 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role(p, base, b, tmem);
     __syncwarp();
+  } else if (warp < 8) {
+    swap_role(p, base, b, tmem, rank, warp, lane);
   } else {
     softmax_role(p, base, b, tmem, rank, warp, lane);
   }
