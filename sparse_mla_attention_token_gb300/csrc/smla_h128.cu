@@ -320,82 +320,125 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
 //   S(g)  = Q_half . K_half(g)^T -> S buffer g%3 (M=128, N=64, K=256: 16 MMAs)
 //   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs,
 //           P(g) read from TMEM buffer g%2, V from the shared-memory stage)
-// in the order S(g+1), PV(g) -- across token boundaries as well -- so the
-// scores of the next tile are on their way while the softmax works.
+// Event-driven: each pass polls (without blocking) whether the next P.V or the
+// next S has its inputs and issues whichever is ready, P.V first because it
+// releases a KV stage.  No operation waits behind another one's inputs.  A
+// pass without progress for ~2 s (or another role giving up) ends the loop.
 __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem) {
   const uint32_t sbase = smem_u32(base);
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTileN, false, false);
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
-  uint32_t gt = 0, qn = 0, tokn = 0;
-  int it = 0;
-  // P.V of a tile is issued two tiles after its S, so the swap and softmax
-  // warpgroups always find the next scores computed.  pend[0] is the older.
-  int pend_g[2] = {-1, -1}, pend_j[2] = {0, 0};
-  uint32_t pend_tok[2] = {0, 0};
+  constexpr int kRing = 8;   // issued-S tiles awaiting their P.V (at most kSBufs + 2)
 
-  auto issue_pv = [&](uint32_t g, int j, uint32_t tk) -> bool {
-    const uint32_t s = g % kStages;
-    if (!wait_bar<false>(bar_addr(b->p_full[g & 1]), (g >> 1) & 1, b, p.err, 2u)) return false;
-    SMLA_TL(1, g, 3);
-    if (j == 0 && !wait_bar<false>(bar_addr(b->o_free), (tk & 1) ^ 1, b, p.err, 2u)) return false;
-    tc_fence_after();
-    const uint32_t kv = sbase + kKVOff + s * kStageBytes;
-    const uint32_t ptm = tmem + kTmemP + (g & 1) * 32;   // P(g) in TMEM: 64 bf16 = 32 columns
-#pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk) {
-      // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart
-      const uint64_t bd = sdesc_sw128(kv + kk * 16 * 128, 8192, 1024);
-      mma_bf16_ts(tmem, ptm + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-    }
-    mma_commit(bar_addr(b->kv_empty[s]));
-    mma_commit(bar_addr(b->pv_done[g & 1]));
-    SMLA_TL(1, g, 4);
-    return true;
-  };
+  // S side: token walk
+  int64_t tok = cid;
+  int it = 0;                 // token iteration (meta slot / parity)
+  int nt = 0, j = 0;          // tiles of the current token, next tile index in it
+  bool have_meta = false, have_q = false;
+  uint32_t qn = 0, tokn = 0;  // tokens with tiles: Q loads consumed, token index
+  uint32_t sg = 0;            // next S tile (global)
+  // P.V side
+  uint32_t pg = 0;            // next P.V tile (global)
+  int ring_j[kRing];
+  uint32_t ring_tok[kRing];
 
-  bool ok = true;
-  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
-    const int slot = it & 1;
-    if (!(ok = wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1, b, p.err, 2u))) break;
-    const int nv = b->nvalid[slot];
-    mbar_arrive(bar_addr(b->meta_empty[slot]));
-    if (nv == 0) continue;
-    if (!(ok = wait_bar<false>(bar_addr(b->q_full), qn & 1, b, p.err, 2u))) break;
-    tc_fence_after();
-    const int ntiles = (nv + kTileN - 1) / kTileN;
-    for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-      const uint32_t s = gt % kStages, ph = (gt / kStages) & 1;
-      const uint32_t sb = gt % kSBufs, sph = (gt / kSBufs) & 1;
-      if (!(ok = wait_bar<false>(bar_addr(b->kv_full[s]), ph, b, p.err, 2u))) break;
-      SMLA_TL(1, gt, 1);
-      if (!(ok = wait_bar<false>(bar_addr(b->s_free[sb]), sph ^ 1, b, p.err, 2u))) break;
-      SMLA_TL(1, gt, 2);
-      tc_fence_after();
-      const uint32_t kv = sbase + kKVOff + s * kStageBytes;
+  long long last = clock64();
+  while (true) {
+    bool progress = false;
+    // ---- next P.V
+    if (pg < sg) {
+      const int jj = ring_j[pg % kRing];
+      const uint32_t tk = ring_tok[pg % kRing];
+      if (mbar_test_wait(bar_addr(b->p_full[pg & 1]), (pg >> 1) & 1) &&
+          (jj != 0 || mbar_test_wait(bar_addr(b->o_free), (tk & 1) ^ 1))) {
+        SMLA_TL(1, pg, 3);
+        tc_fence_after();
+        const uint32_t s = pg % kStages;
+        const uint32_t kv = sbase + kKVOff + s * kStageBytes;
+        const uint32_t ptm = tmem + kTmemP + (pg & 1) * 32;   // P: 64 bf16 = 32 columns
 #pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
-        const uint32_t koff = (kk & 3) * 32;   // 16 K elements = 32 B inside a 128 B row
-        const uint64_t a = sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + koff, 16, 1024);
-        const uint64_t bd = sdesc_sw128(kv + (kk >> 2) * 8192 + koff, 16, 1024);
-        mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart
+          const uint64_t bd = sdesc_sw128(kv + kk * 16 * 128, 8192, 1024);
+          mma_bf16_ts(tmem, ptm + kk * 8, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_addr(b->kv_empty[s]));
+        mma_commit(bar_addr(b->pv_done[pg & 1]));
+        SMLA_TL(1, pg, 4);
+        ++pg;
+        progress = true;
       }
-      mma_commit(bar_addr(b->s_full[sb]));
-      SMLA_TL(1, gt, 0);
-      if (j == ntiles - 1) mma_commit(bar_addr(b->q_empty));
-      if (pend_g[0] >= 0 && !(ok = issue_pv(uint32_t(pend_g[0]), pend_j[0], pend_tok[0]))) break;
-      pend_g[0] = pend_g[1];
-      pend_j[0] = pend_j[1];
-      pend_tok[0] = pend_tok[1];
-      pend_g[1] = static_cast<int>(gt);
-      pend_j[1] = j;
-      pend_tok[1] = tokn;
     }
-    ++qn;
-    ++tokn;
+    // ---- next S (walking tokens; tokens without valid slots have no tiles)
+    if (!progress && tok < p.T && sg - pg < kRing) {
+      if (!have_meta) {
+        const int slot = it & 1;
+        if (mbar_test_wait(bar_addr(b->meta_full[slot]), (it >> 1) & 1)) {
+          const int nv = b->nvalid[slot];
+          mbar_arrive(bar_addr(b->meta_empty[slot]));
+          nt = (nv + kTileN - 1) / kTileN;
+          j = 0;
+          have_meta = true;
+          have_q = false;
+          progress = true;
+          if (nt == 0) {   // nothing to compute for this token
+            have_meta = false;
+            tok += ncl;
+            ++it;
+          }
+        }
+      } else if (!have_q) {
+        if (mbar_test_wait(bar_addr(b->q_full), qn & 1)) {
+          tc_fence_after();
+          have_q = true;
+          progress = true;
+        }
+      } else {
+        const uint32_t s = sg % kStages, ph = (sg / kStages) & 1;
+        const uint32_t sb = sg % kSBufs, sph = (sg / kSBufs) & 1;
+        if (mbar_test_wait(bar_addr(b->kv_full[s]), ph) &&
+            mbar_test_wait(bar_addr(b->s_free[sb]), sph ^ 1)) {
+          SMLA_TL(1, sg, 1);
+          tc_fence_after();
+          const uint32_t kv = sbase + kKVOff + s * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            const uint32_t koff = (kk & 3) * 32;   // 16 K elements = 32 B inside a 128 B row
+            const uint64_t a = sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + koff, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kv + (kk >> 2) * 8192 + koff, 16, 1024);
+            mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar_addr(b->s_full[sb]));
+          SMLA_TL(1, sg, 0);
+          ring_j[sg % kRing] = j;
+          ring_tok[sg % kRing] = tokn;
+          ++sg;
+          progress = true;
+          if (++j == nt) {   // the token's last S: its Q may be replaced
+            mma_commit(bar_addr(b->q_empty));
+            ++qn;
+            ++tokn;
+            have_meta = false;
+            tok += ncl;
+            ++it;
+          }
+        }
+      }
+    }
+    if (tok >= p.T && pg == sg) break;   // every S and every P.V issued
+    if (progress) {
+      last = clock64();
+    } else {
+      if (*reinterpret_cast<volatile int*>(&b->abort_flag)) break;
+      if (clock64() - last > kTimeoutCycles) {
+        *reinterpret_cast<volatile int*>(&b->abort_flag) = 1;
+        atomicOr(p.err, 2u);
+        break;
+      }
+      __nanosleep(32);   // leave issue slots to the warps sharing this sub-partition
+    }
   }
-  for (int k = 0; k < 2 && ok; ++k)
-    if (pend_g[k] >= 0) ok = issue_pv(uint32_t(pend_g[k]), pend_j[k], pend_tok[k]);
   // drain: every MMA issued must complete before TMEM is freed
   mma_commit(bar_addr(b->drain));
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
