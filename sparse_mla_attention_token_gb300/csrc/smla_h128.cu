@@ -19,7 +19,7 @@
 // Data movement.  Producer warp 0 compacts the token's valid slots
 // (0 <= idx < num_kv at the index's full width; PR #6002 "Invalid KV rows",
 // "int64 indices") into a row list and loads the token's Q half with 2-D TMA.
-// Producer warps 0-2 gather each tile's 64 half rows (512 B each) with
+// Producer warps 0-6 gather each tile's 64 half rows (512 B each) with
 // 16-byte cp.async straight into the 128-byte-swizzled layout of a 3-stage
 // ring; each fences its landed copies into the async proxy before it arrives
 // on the stage's barrier.  One tile serves as the K-major B operand of
@@ -33,8 +33,8 @@
 // the running max is only raised when it grows by more than 2^8, which keeps
 // O rescales rare and is exact because O and l use the same stale max.
 //
-// Warps (384 threads): 0-2 producers, 3 TMEM owner + single-thread MMA issuer,
-// 4-7 score swap with the peer CTA, 8-11 softmax + epilogue (thread = TMEM
+// Warps (512 threads): 0-6 producers, 7 TMEM owner + single-thread MMA issuer,
+// 8-11 score swap with the peer CTA, 12-15 softmax + epilogue (thread = TMEM
 // lane = head in both warpgroups).  Every mbarrier wait is
 // bounded: on expiry the kernel sets an error word, every role leaves its
 // loop, in-flight copies and MMAs are drained, TMEM is freed and the kernel
@@ -55,11 +55,13 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 384;
-constexpr int kProducerThreads = 96;  // warps 0-2
-constexpr int kMmaWarp = 3;
-constexpr int kSwapThreads = 128;     // warps 4-7: one thread per head row
-constexpr int kSoftmaxThreads = 128;  // warps 8-11: one thread per head row
+constexpr int kThreads = 512;
+constexpr int kProducerWarps = 7;     // warps 0-6
+constexpr int kProducerThreads = kProducerWarps * 32;
+constexpr int kMmaWarp = 7;
+constexpr int kSoftmaxWarp0 = 12;     // warps 12-15 (swap: 8-11)
+constexpr int kSwapThreads = 128;     // one thread per head row
+constexpr int kSoftmaxThreads = 128;  // one thread per head row
 constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 3;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
@@ -194,7 +196,7 @@ __device__ __forceinline__ void land_and_arrive(uint32_t bar) {
   mbar_arrive(bar);
 }
 
-// Warps 0-2 gather every tile together: warp w copies rows w, w+3, ... (lane c
+// Warps 0-6 gather every tile together: warp w copies rows w, w+7, ... (lane c
 // copies 16-byte chunk c of each 512-byte half row, one contiguous half row
 // per instruction).  Each warp counts its copies on the stage's barrier once
 // they have landed and been fenced into the async proxy, overlapping them with
@@ -280,12 +282,12 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         if (!ok) break;
         SMLA_TL(0, g, 0);
         const uint32_t dst = sbase + kKVOff + s * kStageBytes + chunk_off;
-        // this warp copies rows r = warp + 3k; lane k holds row k's index
-        const int rk = warp + 3 * lane, sl = j * kTileN + rk;
+        // this warp copies rows r = warp + 7k; lane k holds row k's index
+        const int rk = warp + kProducerWarps * lane, sl = j * kTileN + rk;
         const int my_row = (rk < kTileN && sl < nv) ? rows[sl] : -1;
 #pragma unroll
-        for (int k = 0; k < 22; ++k) {
-          const int r = warp + 3 * k;
+        for (int k = 0; k < (kTileN + kProducerWarps - 1) / kProducerWarps; ++k) {
+          const int r = warp + kProducerWarps * k;
           const int rr = __shfl_sync(0xffffffffu, my_row, k);
           if (r < kTileN) {
             const bool valid = rr >= 0;                // the ragged tail is zero-filled
@@ -444,7 +446,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
 }
 
-// Warps 4-7 (128 threads), thread = TMEM lane = head `row`.  For every tile:
+// Warps 8-11 (128 threads), thread = TMEM lane = head `row`.  For every tile:
 //   stage 1(g): read this CTA's partial scores S_r(g) (64 fp32) from TMEM
 //     buffer g%3, round them to fp16 and st.async them into the peer's
 //     receive buffer g%3 (the bytes are counted on the peer's mbarrier);
@@ -467,7 +469,6 @@ __device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t 
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
     xfree_peer[i] = map_peer(bar_addr(b->x_free[i]), peer);
   }
-  uint32_t pend_own[32];
   uint32_t pend_g = 0;
   bool has_pend = false;
 
@@ -477,25 +478,33 @@ __device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t 
     if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]), (g / kXBufs) & 1, b,
                                                 p.err, 8u)))
       return false;
-    uint32_t sfull[64];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(base + (recv_local[xb] - sbase) +
-                                                      ((c ^ (row & 7)) << 4));
-      const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+    for (int h = 0; h < 2; ++h) {
+      // my partial scores are still in S buffer sb (re-read, rounded as when sent)
+      uint32_t sfull[32];
+      tmem_ld32(tl + kTmemS + sb * kTileN + 32 * h, sfull);
+      tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 a = unpack_f16x2(pend_own[4 * c + q]);
-        const float2 e = unpack_f16x2(pv[q]);
-        sfull[8 * c + 2 * q] = __float_as_uint(a.x + e.x);
-        sfull[8 * c + 2 * q + 1] = __float_as_uint(a.y + e.y);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int c = 4 * h + c4;
+        const uint4 v = *reinterpret_cast<const uint4*>(base + (recv_local[xb] - sbase) +
+                                                        ((c ^ (row & 7)) << 4));
+        const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = 8 * c4 + 2 * q;
+          const float2 a = unpack_f16x2(
+              pack_f16x2(__uint_as_float(sfull[i]), __uint_as_float(sfull[i + 1])));
+          const float2 e = unpack_f16x2(pv[q]);
+          sfull[i] = __float_as_uint(a.x + e.x);        // f16(own) + f16(peer)
+          sfull[i + 1] = __float_as_uint(a.y + e.y);
+        }
       }
+      tmem_st32(tl + kTmemS + sb * kTileN + 32 * h, sfull);
     }
     // buffer xb may be refilled: every lane's reads of it have been consumed above
     __syncwarp();
     if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
-    tmem_st32(tl + kTmemS + sb * kTileN, sfull);
-    tmem_st32(tl + kTmemS + sb * kTileN + 32, sfull + 32);
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(bar_addr(b->s_comb[sb]));
@@ -545,15 +554,13 @@ __device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t 
       if (row == 0) SMLA_TL(2, gt, 2);
       if (has_pend && !(ok = combine())) break;
       pend_g = gt;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) pend_own[i] = own[i];
       has_pend = true;
     }
   }
   if (ok && has_pend) combine();
 }
 
-// Warps 8-11 (128 threads), thread = TMEM lane = head `row`.  Per tile: the
+// Warps 12-15 (128 threads), thread = TMEM lane = head `row`.  Per tile: the
 // full scores from TMEM, base-2 online softmax, P (bf16) into TMEM; after a
 // token's last tile the epilogue (sink fold, normalise, bf16 store of this
 // CTA's half of O, lse).
@@ -655,10 +662,13 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
           tmem_st32(tl + 32 * c, o);
         }
       }
-      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-      tmem_st32(tl + kTmemP + pb * 32, pk);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(s[32 * h + 2 * i], s[32 * h + 2 * i + 1]);
+        tmem_st16(tl + kTmemP + pb * 32 + 16 * h, pk);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(b->p_full[pb]));
@@ -751,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role(p, base, b, tmem);
     __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp < kSoftmaxWarp0) {
     swap_role(p, base, b, tmem, rank, warp, lane);
   } else {
     softmax_role(p, base, b, tmem, rank, warp, lane);

@@ -110,6 +110,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint4 v, uint
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
       : "memory");
 }
+// Per-warpgroup register budget changes (all 128 threads of the warpgroup).
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
 // Named barrier among `nthreads` threads (whole warps) of the CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
