@@ -450,10 +450,9 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
 //   stage 1(g): read this CTA's partial scores S_r(g) (64 fp32) from TMEM
 //     buffer g%3, round them to fp16 and st.async them into the peer's
 //     receive buffer g%3 (the bytes are counted on the peer's mbarrier);
-//   stage 2(g-1), one tile later so the swap is in flight meanwhile: add the
-//     peer's fp16 partials to its own, f16(S_0) + f16(S_1) in fp32 (the same
-//     value in both CTAs), write the full scores back into S buffer (g-1)%3 and
-//     hand them to the softmax warpgroup.
+//   stage 2(g), as soon as the peer's partials have arrived: add them to its
+//     own, f16(S_0) + f16(S_1) in fp32 (the same value in both CTAs), write the
+//     full scores back into S buffer g%3 and hand them to the softmax warpgroup.
 __device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
                           uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
@@ -469,12 +468,9 @@ __device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t 
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
     xfree_peer[i] = map_peer(bar_addr(b->x_free[i]), peer);
   }
-  uint32_t pend_g = 0;
-  bool has_pend = false;
-
-  // stage 2 of the pending tile
-  auto combine = [&]() -> bool {
-    const uint32_t g = pend_g, xb = g % kXBufs, sb = g % kSBufs;
+  // stage 2 of tile g: add the peer's partials to mine, full scores back to TMEM
+  auto combine = [&](uint32_t g) -> bool {
+    const uint32_t xb = g % kXBufs, sb = g % kSBufs;
     if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]), (g / kXBufs) & 1, b,
                                                 p.err, 8u)))
       return false;
@@ -512,52 +508,110 @@ __device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t 
     return true;
   };
 
-  uint32_t gt = 0;
-  int it = 0;
+  // stage 1 of tile g: my partial scores out of TMEM, fp16, to the peer
+  auto send = [&](uint32_t g) -> bool {
+    const uint32_t sb = g % kSBufs, xb = g % kXBufs;
+    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]), (g / kSBufs) & 1,
+                                                 b, p.err, 8u)))
+      return false;
+    tc_fence_after();
+    uint32_t own[32];
+    {
+      uint32_t sv[64];
+      tmem_ld32(tl + kTmemS + sb * kTileN, sv);
+      tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+    }
+    if (row == 0) SMLA_TL(2, g, 1);
+    // the peer has consumed what I sent into its buffer xb three tiles ago
+    if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_free[xb]),
+                                                ((g / kXBufs) & 1) ^ 1, b, p.err, 8u)))
+      return false;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      st_async_v4(recv_peer[xb] + ((c ^ (row & 7)) << 4),
+                  make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
+                  xfull_peer[xb]);
+    if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
+    if (row == 0) SMLA_TL(2, g, 2);
+    return true;
+  };
+
+  // Event-driven: combine the oldest sent tile as soon as the peer's partials
+  // are in (that unblocks the softmax), otherwise send the next tile as soon
+  // as its partial scores are in TMEM.  Decisions are warp-uniform (lane 0's
+  // non-blocking test, broadcast); the waits inside return at once.
+  int64_t tok = cid;
+  int it = 0, nt = 0, j = 0;
+  bool have_meta = false;
+  uint32_t g1 = 0, g2 = 0;   // next tile to send / to combine
+  long long last = clock64();
   bool ok = true;
-  for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
-    const int slot = it & 1;
-    ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]), (it >> 1) & 1,
-                                                 b, p.err, 8u));
-    if (!ok) break;
-    const int nv = b->nvalid[slot];
-    mbar_arrive(bar_addr(b->meta_empty[slot]));
-    const int ntiles = (nv + kTileN - 1) / kTileN;
-    for (int j = 0; j < ntiles; ++j, ++gt) {
-      const uint32_t sb = gt % kSBufs, xb = gt % kXBufs;
-      if (row == 0) SMLA_TL(2, gt, 0);
-      if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]),
-                                                         (gt / kSBufs) & 1, b, p.err, 8u))))
-        break;
-      tc_fence_after();
-      uint32_t own[32];
-      {
-        uint32_t sv[64];
-        tmem_ld32(tl + kTmemS + sb * kTileN, sv);
-        tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+  while (ok) {
+    bool progress = false;
+    if (g2 < g1) {
+      const bool ready = __shfl_sync(
+          0xffffffffu,
+          lane == 0 ? mbar_test_wait(bar_addr(b->x_full[g2 % kXBufs]), (g2 / kXBufs) & 1) : false, 0);
+      if (ready) {
+        ok = combine(g2);
+        ++g2;
+        progress = true;
       }
-      if (row == 0) SMLA_TL(2, gt, 1);
-      // the peer has consumed what I sent into its buffer xb three tiles ago
-      if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_free[xb]),
-                                                        ((gt / kXBufs) & 1) ^ 1, b, p.err, 8u))))
+    }
+    if (ok && !progress && tok < p.T) {
+      if (!have_meta) {
+        const int slot = it & 1;
+        const bool ready = __shfl_sync(
+            0xffffffffu,
+            lane == 0 ? mbar_test_wait(bar_addr(b->meta_full[slot]), (it >> 1) & 1) : false, 0);
+        if (ready) {
+          ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]),
+                                                       (it >> 1) & 1, b, p.err, 8u));
+          const int nv = b->nvalid[slot];
+          mbar_arrive(bar_addr(b->meta_empty[slot]));
+          nt = (nv + kTileN - 1) / kTileN;
+          j = 0;
+          have_meta = nt > 0;
+          if (nt == 0) {
+            tok += ncl;
+            ++it;
+          }
+          progress = true;
+        }
+      } else {
+        const bool ready = __shfl_sync(
+            0xffffffffu,
+            lane == 0 ? mbar_test_wait(bar_addr(b->s_full[g1 % kSBufs]), (g1 / kSBufs) & 1)
+                      : false, 0);
+        if (ready) {
+          ok = send(g1);
+          ++g1;
+          progress = true;
+          if (++j == nt) {
+            have_meta = false;
+            tok += ncl;
+            ++it;
+          }
+        }
+      }
+    }
+    if (tok >= p.T && g2 == g1) break;
+    if (progress) {
+      last = clock64();
+    } else {
+      if (*reinterpret_cast<volatile int*>(&b->abort_flag)) break;
+      if (clock64() - last > kTimeoutCycles) {
+        *reinterpret_cast<volatile int*>(&b->abort_flag) = 1;
+        atomicOr(p.err, 8u);
         break;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(recv_peer[xb] + ((c ^ (row & 7)) << 4),
-                    make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
-                    xfull_peer[xb]);
-      if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
-      if (row == 0) SMLA_TL(2, gt, 2);
-      if (has_pend && !(ok = combine())) break;
-      pend_g = gt;
-      has_pend = true;
+      }
+      __nanosleep(32);
     }
   }
-  if (ok && has_pend) combine();
 }
 
 // Warps 12-15 (128 threads), thread = TMEM lane = head `row`.  Per tile: the
