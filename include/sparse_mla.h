@@ -165,6 +165,16 @@ smla_status_t sparse_mla_launch_config(int64_t T, int32_t H, int32_t topk, int64
  */
 smla_status_t sparse_mla_device_status(void* stream);
 
+/*
+ * sparse_mla_selftest_wait_timeout -- exercise the failure-detection path.
+ * Queues on `stream` a one-thread kernel whose bounded mbarrier wait can never
+ * be satisfied: after ~1 ms it records the expiry in the library's device
+ * error word and returns normally (no fault, no trap; the context stays
+ * usable).  The next sparse_mla_device_status on that device then returns
+ * SMLA_ERR_DEVICE_TIMEOUT and clears the word.  For tests and health checks.
+ */
+smla_status_t sparse_mla_selftest_wait_timeout(void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* sparse_mla_strerror(int32_t status);
 

@@ -41,6 +41,7 @@ SIGNATURES = {
     "sparse_mla_plan": (_I32, [_I64, _I32, _I32, _I32, _P, _P, _P]),
     "sparse_mla_launch_config": (_I32, [_I64, _I32, _I32, _I64, _I32, _P, _P, _P, _P]),
     "sparse_mla_device_status": (_I32, [_P]),
+    "sparse_mla_selftest_wait_timeout": (_I32, [_P]),
     "sparse_mla_strerror": (ctypes.c_char_p, [_I32]),
     "sparse_mla_last_cuda_error": (ctypes.c_char_p, []),
     "sparse_mla_abi_version": (_I32, []),
@@ -192,6 +193,13 @@ def sparse_mla_fwd(q, kv, topk_indices, attn_sink=None, scale: Optional[float] =
     if st != SMLA_OK:
         raise SparseMLAError(st, "sparse_mla_fwd")
     return out, lse
+
+
+def sparse_mla_selftest_wait_timeout(stream=None) -> None:
+    """Queue the bounded-wait self-test (its wait always expires after ~1 ms)."""
+    st = lib().sparse_mla_selftest_wait_timeout(_stream_ptr(stream))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_selftest_wait_timeout")
 
 
 def sparse_mla_device_status(stream=None) -> int:

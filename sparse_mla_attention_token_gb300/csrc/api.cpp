@@ -257,6 +257,12 @@ smla_status_t sparse_mla_launch_config(int64_t T, int32_t H, int32_t topk, int64
   return SMLA_OK;
 }
 
+smla_status_t sparse_mla_selftest_wait_timeout(void* stream) {
+  const int e = smla::selftest_wait_timeout(stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "self-test launch");
+  return SMLA_OK;
+}
+
 smla_status_t sparse_mla_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

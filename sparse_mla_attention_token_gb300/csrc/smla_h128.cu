@@ -948,7 +948,32 @@ cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Self-test of the bounded-wait path: one thread waits on an mbarrier that
+// nothing ever arrives at, gives up after `limit` cycles, records the expiry
+// in the same error word the H=128 kernel uses and returns.
+__global__ void wait_timeout_selftest_kernel(unsigned int* err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t a = smem_u32(&bar);
+  mbar_init(a, 1);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, 0)) {
+    if (clock64() - t0 > limit) {
+      atomicOr(err, 16u);
+      return;
+    }
+  }
+}
+
 }  // namespace
+
+int selftest_wait_timeout(void* stream) {
+  unsigned int* err = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_h128_error);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, 2000000LL);
+  return static_cast<int>(cudaGetLastError());
+}
 
 bool h128_supported(int64_t T, int32_t H, int32_t topk, int64_t num_kv) {
   return H == 128 && topk >= 1 && topk <= kMaxTopk && num_kv >= 1 && T >= 1 &&

@@ -44,6 +44,8 @@ bool h128_supported(int64_t T, int32_t H, int32_t topk, int64_t num_kv);
 #ifdef SMLA_TIMELINE
 int h128_timeline(long long* host);
 #endif
+// Launch the bounded-wait self-test kernel (its wait always expires).
+int selftest_wait_timeout(void* stream);
 // Device address of the h128 kernel's error word (bounded waits), or nullptr.
 int h128_error_word(unsigned int** addr);
 
