@@ -65,6 +65,60 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
+// The same widening on the integer and FMA pipes (no conversion unit), for
+// finite fp16 values: the 15 exponent+mantissa bits move to the top of an
+// fp32 mantissa-aligned field (an fp32 whose exponent is 112 too small; fp16
+// subnormals land on fp32 subnormals) and one exact multiply by 2^112
+// restores the exponent.  Needs the default no-flush-to-zero multiply.
+__device__ __forceinline__ float2 unpack_f16x2_alu(uint32_t v) {
+  const uint32_t lo = ((v & 0x7FFFu) << 13) | ((v & 0x8000u) << 16);
+  const uint32_t hi = ((v >> 3) & 0x0FFFE000u) | (v & 0x80000000u);
+  return make_float2(__uint_as_float(lo) * 0x1p112f, __uint_as_float(hi) * 0x1p112f);
+}
+
+// f16(a) + f16(b) in fp32 for both halves of two packed fp16x2 words: each
+// half of b is widened exactly (b + 0), then added to the matching half of a
+// with one fp32 rounding (mixed-precision add, sm_100 family).
+__device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
+  float2 r;
+  asm("{\n.reg .f16 a0, a1, b0, b1;\n.reg .f32 t0, t1;\n"
+      "mov.b32 {a0, a1}, %2;\n"
+      "mov.b32 {b0, b1}, %3;\n"
+      "add.rn.f32.f16 t0, b0, 0f00000000;\n"
+      "add.rn.f32.f16 t1, b1, 0f00000000;\n"
+      "add.rn.f32.f16 %0, a0, t0;\n"
+      "add.rn.f32.f16 %1, a1, t1;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(a), "r"(b));
+  return r;
+}
+// Packed fp32 pair arithmetic (one instruction for two lanes of work, sm_100 family).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n.reg .b64 x, y, z;\n"
+      "mov.b64 x, {%2, %3};\nmov.b64 y, {%4, %5};\n"
+      "mul.rn.f32x2 z, x, y;\n"
+      "mov.b64 {%0, %1}, z;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n.reg .b64 x, y, z;\n"
+      "mov.b64 x, {%2, %3};\nmov.b64 y, {%4, %5};\n"
+      "add.rn.f32x2 z, x, y;\n"
+      "mov.b64 {%0, %1}, z;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+// max of three floats in one instruction (sm_100 family)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 // The hardware base-2 exponential (MUFU.EX2): ex2.approx.ftz.f32.
 __device__ __forceinline__ float ex2(float x) {

@@ -59,9 +59,8 @@ constexpr int kThreads = 512;
 constexpr int kProducerWarps = 7;     // warps 0-6
 constexpr int kProducerThreads = kProducerWarps * 32;
 constexpr int kMmaWarp = 7;
-constexpr int kSoftmaxWarp0 = 12;     // warps 12-15 (swap: 8-11)
-constexpr int kSwapThreads = 128;     // one thread per head row
-constexpr int kSoftmaxThreads = 128;  // one thread per head row
+constexpr int kScoreWarp0 = 8;        // warps 8-15: two score warpgroups
+constexpr int kWgThreads = 128;       // one thread per head row
 constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 3;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
@@ -75,11 +74,15 @@ constexpr uint32_t kQOff = 0;                         // [4 col blocks][128 rows
 constexpr uint32_t kQBytes = 128 * 256 * 2;           // 64 KB
 constexpr uint32_t kKVOff = kQOff + kQBytes;          // [stage][4 col blocks][64 rows][128 B]
 constexpr uint32_t kStageBytes = kTileN * 256 * 2;    // 32 KB
-constexpr uint32_t kXOff = kKVOff + kStages * kStageBytes;   // peer partials: [3][128][64 fp16]
-constexpr int kXBufs = 3;
+constexpr uint32_t kXOff = kKVOff + kStages * kStageBytes;   // peer partials: [2][128][64 fp16]
+constexpr int kXBufs = 2;
 constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
-constexpr uint32_t kRowsOff = kXOff + kXBufs * kXBufBytes;   // int32 row lists
-constexpr uint32_t kBarOff = kRowsOff + 2 * kMaxTopk * 4;
+constexpr uint32_t kStgOff = kXOff + kXBufs * kXBufBytes;    // O store staging: [8 warps][32][32 bf16]
+constexpr uint32_t kStgBytes = 32 * 32 * 2;                  // 2 KB per score warp
+constexpr uint32_t kRowsOff = kStgOff + 8 * kStgBytes;       // int32 row lists
+constexpr uint32_t kMaxOff = kRowsOff + 2 * kMaxTopk * 4;    // running max handoff [2][128]
+constexpr uint32_t kSumOff = kMaxOff + 2 * 128 * 4;          // epilogue sums [2][2][2][128]
+constexpr uint32_t kBarOff = kSumOff + 2 * 512 * 4;
 constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
 
 constexpr long long kTimeoutCycles = 4000000000LL;    // ~2 s at 2 GHz
@@ -88,8 +91,9 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[kSBufs];   // partial S(g) in TMEM (MMA commit)
-  uint64_t s_comb[kSBufs];   // full S(g) written back by the swap warpgroup
-  uint64_t s_free[kSBufs];   // the softmax has read S(g)
+  uint64_t s_free[kSBufs];   // the score warpgroup has read S(g)
+  uint64_t m_ready[2][4];    // running max of tile g published (per tile parity, per quadrant)
+  uint64_t epi;              // both score warpgroups have published their sums
   uint64_t p_full[2], pv_done[2];   // per P buffer
   uint64_t x_full[kXBufs], x_free[kXBufs];
   uint64_t o_free;
@@ -120,14 +124,19 @@ struct H128Params {
 
 __device__ unsigned int g_h128_error;
 
-// Optional per-role timeline of cluster 0 (clock64 per event, first 64 tiles),
-// compiled only with -DSMLA_TIMELINE for performance investigations.
+// Optional per-role timeline of cluster 0 (clock64 per event, 64 tiles from
+// tile SMLA_TL_START), compiled only with -DSMLA_TIMELINE for performance
+// investigations.
 #ifdef SMLA_TIMELINE
+#ifndef SMLA_TL_START
+#define SMLA_TL_START 0
+#endif
 __device__ long long g_timeline[2][4][64][8];
-#define SMLA_TL(role, g, ev)                                             \
-  do {                                                                   \
-    if (cluster_id_x() == 0 && (g) < 64)                                 \
-      g_timeline[cluster_ctarank()][role][g][ev] = clock64();            \
+#define SMLA_TL(role, g, ev)                                                        \
+  do {                                                                              \
+    const uint32_t tl_g_ = static_cast<uint32_t>(g) - SMLA_TL_START;                \
+    if (cluster_id_x() == 0 && tl_g_ < 64u)                                         \
+      g_timeline[cluster_ctarank()][role][tl_g_][ev] = clock64();                   \
   } while (0)
 #else
 #define SMLA_TL(role, g, ev) \
@@ -236,9 +245,11 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         mbar_arrive(bar_addr(b->meta_full[slot]));
       }
       if (ok && nv > 0) {
+        if (lane == 0) SMLA_TL(0, gt, 4);
         ok = __all_sync(0xffffffffu,
                         wait_bar<false>(bar_addr(b->q_empty), (qn & 1) ^ 1, b, p.err, 1u));
         if (ok && lane == 0) {
+          SMLA_TL(0, gt, 3);
           mbar_arrive_expect_tx(bar_addr(b->q_full), kQBytes);
 #pragma unroll
           for (int cb = 0; cb < 4; ++cb)
@@ -280,7 +291,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         const bool ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->kv_empty[s]),
                                                                 ph ^ 1, b, p.err, 1u));
         if (!ok) break;
-        SMLA_TL(0, g, 0);
+        if (lane == 0) SMLA_TL(0, g, 0);
         const uint32_t dst = sbase + kKVOff + s * kStageBytes + chunk_off;
         // this warp copies rows r = warp + 7k; lane k holds row k's index
         const int rk = warp + kProducerWarps * lane, sl = j * kTileN + rk;
@@ -296,18 +307,19 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
           }
         }
         cp_async_commit();
-        SMLA_TL(0, g, 1);
+        if (lane == 0) SMLA_TL(0, g, 1);
         if (!compacted && j == ntiles - 1) compact_next();   // overlaps the copies
         if (pending >= 0) {
           cp_async_wait<1>();
           land_and_arrive(bar_addr(b->kv_full[pending]));
+          if (lane == 0) SMLA_TL(0, g - 1, 2);
         }
         pending = static_cast<int>(s);
       }
       if (pending >= 0) {
         cp_async_wait<0>();
         land_and_arrive(bar_addr(b->kv_full[pending]));
-        SMLA_TL(0, gt + ntiles - 1, 2);
+        if (lane == 0) SMLA_TL(0, gt + ntiles - 1, 2);
       }
       gt += ntiles;
     }
@@ -392,6 +404,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
         }
       } else if (!have_q) {
         if (mbar_test_wait(bar_addr(b->q_full), qn & 1)) {
+          SMLA_TL(1, sg, 5);
           tc_fence_after();
           have_q = true;
           progress = true;
@@ -446,20 +459,38 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
 }
 
-// Warps 8-11 (128 threads), thread = TMEM lane = head `row`.  For every tile:
-//   stage 1(g): read this CTA's partial scores S_r(g) (64 fp32) from TMEM
-//     buffer g%3, round them to fp16 and st.async them into the peer's
-//     receive buffer g%3 (the bytes are counted on the peer's mbarrier);
-//   stage 2(g), as soon as the peer's partials have arrived: add them to its
-//     own, f16(S_0) + f16(S_1) in fp32 (the same value in both CTAs), write the
-//     full scores back into S buffer g%3 and hand them to the softmax warpgroup.
-__device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
-                          uint32_t rank, int warp, int lane) {
+// Warps 8-15: two score warpgroups.  Warpgroup w handles the tiles g with
+// g % 2 == w (tile numbers count every tile of this CTA); thread = TMEM lane =
+// head `row`.  For its tile g a warpgroup
+//   1. reads this CTA's partial scores S_r(g) (64 fp32) from S buffer g%3,
+//      rounds them to fp16 and frees the buffer;
+//   2. st.asyncs them into the peer's receive buffer g%3 (the bytes are
+//      counted on the peer's mbarrier);
+//   3. once the peer's partials are in, forms S = f16(S_0) + f16(S_1) in fp32
+//      (the same value in both CTAs);
+//   4. takes the running max: it waits for the max the other warpgroup
+//      settled for tile g-1 (per row, through shared memory), raises it only
+//      when the tile's max exceeds it by more than 2^8, and publishes it for
+//      tile g+1;
+//   5. writes P = 2^(S - m) (bf16) into TMEM P buffer g%2 and, when the max
+//      was raised, first rescales O (after P.V(g-1) has completed).
+// Each warpgroup keeps the sum l of its own tiles (relative to the max it last
+// saw); at the end of a token the two sums are merged through shared memory
+// and the warpgroups normalise and store one half each of this CTA's O half.
+__device__ void score_role(const H128Params& p, const CUtensorMap* tm_o, uint8_t* base, Bars* b,
+                           uint32_t tmem, uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
-  const int row = 32 * (warp & 3) + lane;
-  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
+  const int wg = (warp - kScoreWarp0) >> 2;   // 0 or 1
+  const int qd = warp & 3;                    // TMEM lane quadrant
+  const int row = 32 * qd + lane;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   const uint32_t peer = rank ^ 1u;
+  const float sl2 = p.scale * kLog2e;
+  const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
+  float* m_sh = reinterpret_cast<float*>(base + kMaxOff);   // [2 tile parities][128]
+  float* l_sh = reinterpret_cast<float*>(base + kSumOff);   // [2 tokens][2 wg][2 (l, m)][128]
+  const uint32_t stg = sbase + kStgOff + (warp - kScoreWarp0) * kStgBytes;
   uint32_t recv_local[kXBufs], recv_peer[kXBufs], xfull_peer[kXBufs], xfree_peer[kXBufs];
 #pragma unroll
   for (int i = 0; i < kXBufs; ++i) {
@@ -468,166 +499,8 @@ __device__ void swap_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t 
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
     xfree_peer[i] = map_peer(bar_addr(b->x_free[i]), peer);
   }
-  // stage 2 of tile g: add the peer's partials to mine, full scores back to TMEM
-  auto combine = [&](uint32_t g) -> bool {
-    const uint32_t xb = g % kXBufs, sb = g % kSBufs;
-    if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]), (g / kXBufs) & 1, b,
-                                                p.err, 8u)))
-      return false;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      // my partial scores are still in S buffer sb (re-read, rounded as when sent)
-      uint32_t sfull[32];
-      tmem_ld32(tl + kTmemS + sb * kTileN + 32 * h, sfull);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int c = 4 * h + c4;
-        const uint4 v = *reinterpret_cast<const uint4*>(base + (recv_local[xb] - sbase) +
-                                                        ((c ^ (row & 7)) << 4));
-        const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i = 8 * c4 + 2 * q;
-          const float2 a = unpack_f16x2(
-              pack_f16x2(__uint_as_float(sfull[i]), __uint_as_float(sfull[i + 1])));
-          const float2 e = unpack_f16x2(pv[q]);
-          sfull[i] = __float_as_uint(a.x + e.x);        // f16(own) + f16(peer)
-          sfull[i + 1] = __float_as_uint(a.y + e.y);
-        }
-      }
-      tmem_st32(tl + kTmemS + sb * kTileN + 32 * h, sfull);
-    }
-    // buffer xb may be refilled: every lane's reads of it have been consumed above
-    __syncwarp();
-    if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(bar_addr(b->s_comb[sb]));
-    if (row == 0) SMLA_TL(3, g, 1);
-    return true;
-  };
 
-  // stage 1 of tile g: my partial scores out of TMEM, fp16, to the peer
-  auto send = [&](uint32_t g) -> bool {
-    const uint32_t sb = g % kSBufs, xb = g % kXBufs;
-    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]), (g / kSBufs) & 1,
-                                                 b, p.err, 8u)))
-      return false;
-    tc_fence_after();
-    uint32_t own[32];
-    {
-      uint32_t sv[64];
-      tmem_ld32(tl + kTmemS + sb * kTileN, sv);
-      tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        own[i] = pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
-    }
-    if (row == 0) SMLA_TL(2, g, 1);
-    // the peer has consumed what I sent into its buffer xb three tiles ago
-    if (!__all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_free[xb]),
-                                                ((g / kXBufs) & 1) ^ 1, b, p.err, 8u)))
-      return false;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      st_async_v4(recv_peer[xb] + ((c ^ (row & 7)) << 4),
-                  make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
-                  xfull_peer[xb]);
-    if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
-    if (row == 0) SMLA_TL(2, g, 2);
-    return true;
-  };
-
-  // Event-driven: combine the oldest sent tile as soon as the peer's partials
-  // are in (that unblocks the softmax), otherwise send the next tile as soon
-  // as its partial scores are in TMEM.  Decisions are warp-uniform (lane 0's
-  // non-blocking test, broadcast); the waits inside return at once.
-  int64_t tok = cid;
-  int it = 0, nt = 0, j = 0;
-  bool have_meta = false;
-  uint32_t g1 = 0, g2 = 0;   // next tile to send / to combine
-  long long last = clock64();
-  bool ok = true;
-  while (ok) {
-    bool progress = false;
-    if (g2 < g1) {
-      const bool ready = __shfl_sync(
-          0xffffffffu,
-          lane == 0 ? mbar_test_wait(bar_addr(b->x_full[g2 % kXBufs]), (g2 / kXBufs) & 1) : false, 0);
-      if (ready) {
-        ok = combine(g2);
-        ++g2;
-        progress = true;
-      }
-    }
-    if (ok && !progress && tok < p.T) {
-      if (!have_meta) {
-        const int slot = it & 1;
-        const bool ready = __shfl_sync(
-            0xffffffffu,
-            lane == 0 ? mbar_test_wait(bar_addr(b->meta_full[slot]), (it >> 1) & 1) : false, 0);
-        if (ready) {
-          ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_full[slot]),
-                                                       (it >> 1) & 1, b, p.err, 8u));
-          const int nv = b->nvalid[slot];
-          mbar_arrive(bar_addr(b->meta_empty[slot]));
-          nt = (nv + kTileN - 1) / kTileN;
-          j = 0;
-          have_meta = nt > 0;
-          if (nt == 0) {
-            tok += ncl;
-            ++it;
-          }
-          progress = true;
-        }
-      } else {
-        const bool ready = __shfl_sync(
-            0xffffffffu,
-            lane == 0 ? mbar_test_wait(bar_addr(b->s_full[g1 % kSBufs]), (g1 / kSBufs) & 1)
-                      : false, 0);
-        if (ready) {
-          ok = send(g1);
-          ++g1;
-          progress = true;
-          if (++j == nt) {
-            have_meta = false;
-            tok += ncl;
-            ++it;
-          }
-        }
-      }
-    }
-    if (tok >= p.T && g2 == g1) break;
-    if (progress) {
-      last = clock64();
-    } else {
-      if (*reinterpret_cast<volatile int*>(&b->abort_flag)) break;
-      if (clock64() - last > kTimeoutCycles) {
-        *reinterpret_cast<volatile int*>(&b->abort_flag) = 1;
-        atomicOr(p.err, 8u);
-        break;
-      }
-      __nanosleep(32);
-    }
-  }
-}
-
-// Warps 12-15 (128 threads), thread = TMEM lane = head `row`.  Per tile: the
-// full scores from TMEM, base-2 online softmax, P (bf16) into TMEM; after a
-// token's last tile the epilogue (sink fold, normalise, bf16 store of this
-// CTA's half of O, lse).
-__device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
-                             uint32_t rank, int warp, int lane) {
-  const int row = 32 * (warp & 3) + lane;
-  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // lane quadrant
-  const int64_t cid = cluster_id_x(), ncl = nclusters_x();
-  const float sl2 = p.scale * kLog2e;
-  const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
-  (void)base;
-
-  uint32_t gt = 0;
+  uint32_t gt = 0, et = 0;   // tiles before this token; tokens with tiles so far
   int it = 0;
   bool ok = true;
   for (int64_t tok = cid; tok < p.T && ok; tok += ncl, ++it) {
@@ -637,25 +510,28 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
     if (!ok) break;
     const int nv = b->nvalid[slot];
     mbar_arrive(bar_addr(b->meta_empty[slot]));
+    // this warpgroup's 128 columns of the CTA's 256-column O half (empty tokens only)
     uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
-                                           256 * rank);
+                                           256 * rank + 128 * wg);
     if (nv == 0) {   // nothing valid: O = 0; lse = sink (finite) or -inf
 #pragma unroll
-      for (int c = 0; c < 32; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-      if (rank == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
+      for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (rank == 0 && wg == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
       continue;
     }
-    float m_run = -INFINITY, l_run = 0.f;
     const int ntiles = (nv + kTileN - 1) / kTileN;
-    for (int j = 0; j < ntiles; ++j, ++gt) {
-      const uint32_t g = gt, sb = g % kSBufs, pb = g & 1;
-      if (row == 0) SMLA_TL(3, g, 2);
-      if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_comb[sb]),
-                                                         (g / kSBufs) & 1, b, p.err, 4u))))
+    float l_w = 0.f, m_lw = -INFINITY;   // this warpgroup's sum and the max it is relative to
+    for (int j = 0; j < ntiles; ++j) {
+      const uint32_t g = gt + j;
+      if (static_cast<int>(g & 1u) != wg) continue;
+      const uint32_t sb = g % kSBufs, xb = g % kXBufs, pb = g & 1;
+      // 1. my partial scores, rounded to fp16; the S buffer is free again
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]),
+                                                         (g / kSBufs) & 1, b, p.err, 8u))))
         break;
-      if (row == 0) SMLA_TL(3, g, 3);
+      if (row == 0) SMLA_TL(2, g, 0);
       tc_fence_after();
-      float s[64];
+      uint32_t own[32];
       {
         uint32_t sv[64];
         tmem_ld32(tl + kTmemS + sb * kTileN, sv);
@@ -663,37 +539,95 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar_addr(b->s_free[sb]));
+        // scaled to base-2 logits before the rounding (keeps fp16's range for large scores)
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sv[i]);
+        for (int i = 0; i < 32; ++i) {
+          const float2 t = mul2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                make_float2(sl2, sl2));
+          own[i] = pack_f16x2(t.x, t.y);
+        }
       }
-      // online softmax, base 2; columns past the valid count are -inf
+      if (row == 0) SMLA_TL(3, g, 0);
+      // 2. to the peer, once it has consumed what it got in buffer xb two tiles ago
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_free[xb]),
+                                                        ((g / kXBufs) & 1) ^ 1, b, p.err, 8u))))
+        break;
+      if (row == 0) SMLA_TL(3, g, 1);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(recv_peer[xb] + ((c ^ (row & 7)) << 4),
+                    make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
+                    xfull_peer[xb]);
+      if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
+      if (row == 0) SMLA_TL(2, g, 1);
+      // 3. the peer's partial scores; full base-2 scores, tail masked
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]),
+                                                        (g / kXBufs) & 1, b, p.err, 8u))))
+        break;
+      if (row == 0) SMLA_TL(2, g, 2);
       const int nvt = min(kTileN, nv - j * kTileN);
-      float mx8[8];
+      float s[64];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(base + (recv_local[xb] - sbase) +
+                                                        ((c ^ (row & 7)) << 4));
+        const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        s[i] = (i < nvt) ? s[i] * sl2 : -INFINITY;
-        mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+        for (int q = 0; q < 4; ++q) {
+          const float2 t = add_f16x2_f32(own[4 * c + q], pv[q]);   // f16(own) + f16(peer)
+          s[8 * c + 2 * q] = t.x;
+          s[8 * c + 2 * q + 1] = t.y;
+        }
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const bool need = mx > m_run + 8.f;   // raise the max only when it grows past 2^8
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_run - mx);
-        m_run = mx;
-      }
-      float sum8[8];
+      if (nvt < kTileN) {   // the token's ragged last tile
 #pragma unroll
-      for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        s[i] = ex2(s[i] - m_run);
-        sum8[i & 7] += s[i];
+        for (int i = 0; i < 64; ++i) s[i] = (i < nvt) ? s[i] : -INFINITY;
       }
-      l_run = l_run * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+      if (row == 0) SMLA_TL(3, g, 2);
+      // 4. running max: the one settled for tile g-1 (also across tokens, so that
+      //    its slot is read before it is written again), raised by more than 2^8 only
+      float mx;
+      {
+        float t[22];
+#pragma unroll
+        for (int k = 0; k < 21; ++k) t[k] = max3f(s[3 * k], s[3 * k + 1], s[3 * k + 2]);
+        t[21] = s[63];
+        float u[8];
+#pragma unroll
+        for (int k = 0; k < 7; ++k) u[k] = max3f(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
+        u[7] = t[21];
+        mx = max3f(max3f(u[0], u[1], u[2]), max3f(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+      }
+      float m_prev = -INFINITY;
+      if (g >= 1) {
+        if (!(ok = __all_sync(0xffffffffu,
+                              wait_bar<false>(bar_addr(b->m_ready[(g - 1) & 1][qd]),
+                                              ((g - 1) >> 1) & 1, b, p.err, 4u))))
+          break;
+        if (j > 0) m_prev = m_sh[((g - 1) & 1) * 128 + row];
+      }
+      if (row == 0) SMLA_TL(3, g, 3);
+      const bool need = mx > m_prev + 8.f;
+      const float m_new = need ? mx : m_prev;
+      m_sh[(g & 1) * 128 + row] = m_new;
+      mbar_arrive(bar_addr(b->m_ready[g & 1][qd]));
+      if (row == 0) SMLA_TL(2, g, 3);
+      // 5. P = 2^(S - m), this warpgroup's sum
+      float2 sum4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sum4[k] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float2 t = add2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(-m_new, -m_new));
+        t.x = ex2(t.x);
+        t.y = ex2(t.y);
+        s[2 * i] = t.x;
+        s[2 * i + 1] = t.y;
+        sum4[i & 3] = add2(sum4[i & 3], t);
+      }
+      const float2 sa = add2(add2(sum4[0], sum4[1]), add2(sum4[2], sum4[3]));
+      l_w = l_w * ex2(m_lw - m_new) + (sa.x + sa.y);
+      m_lw = m_new;
       // P buffer pb was last read by P.V(g-2); O may only be rescaled after P.V(g-1)
       if (g >= 2) {
         if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb]),
@@ -706,6 +640,7 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
                                                            ((g - 1) >> 1) & 1, b, p.err, 4u))))
           break;
         tc_fence_after();
+        const float alpha = ex2(m_prev - m_new);   // 1 for rows whose max stayed
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           uint32_t o[32];
@@ -716,6 +651,7 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
           tmem_st32(tl + 32 * c, o);
         }
       }
+      if (row == 0) SMLA_TL(3, g, 4);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[16];
@@ -726,14 +662,30 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(b->p_full[pb]));
-      if (row == 0) SMLA_TL(3, g, 4);
+      // receive buffer xb may be refilled: every lane's reads of it were consumed above
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
+      if (row == 0) SMLA_TL(2, g, 4);
     }
     if (!ok) break;
-    // epilogue: wait for the token's last P.V, fold the sink, normalise, store
+    gt += ntiles;
+    // epilogue: merge the two warpgroups' sums, wait for the token's last P.V,
+    // fold the sink, normalise, store this warpgroup's 128 columns
+    float* lsh = l_sh + (et & 1) * 512;
+    lsh[wg * 256 + row] = l_w;
+    lsh[wg * 256 + 128 + row] = m_lw;
+    mbar_arrive(bar_addr(b->epi));
+    if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->epi), et & 1, b, p.err, 4u))))
+      break;
+    const float l_o = lsh[(wg ^ 1) * 256 + row], m_o = lsh[(wg ^ 1) * 256 + 128 + row];
+    ++et;
+    const float m_run = fmaxf(m_lw, m_o);   // the max of the token's last tile
+    const float l_run = l_w * ex2(m_lw - m_run) + l_o * ex2(m_o - m_run);
     const uint32_t gl = gt - 1;
     if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[gl & 1]),
                                                        (gl >> 1) & 1, b, p.err, 4u))))
       break;
+    if (row == 0) SMLA_TL(3, gl, 5);
     tc_fence_after();
     float m2 = m_run, l2 = l_run;
     if (sk != -INFINITY) {
@@ -741,11 +693,16 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
       l2 = l_run * ex2(m_run - m2) + ex2(sk - m2);
     }
     const float f = ex2(m_run - m2) / l2;
+    // 32 x 32 bf16 blocks through this warp's staging buffer (64-byte rows,
+    // 64-byte swizzle: 16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3)),
+    // written to global memory by TMA (whole lines instead of 32 rows per store)
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
-      tmem_ld32(tl + 32 * c, o);
+      tmem_ld32(tl + 128 * wg + 32 * c, o);
       tmem_wait_ld();
+      if (lane == 0) bulk_wait_read<0>();   // the previous block has left the buffer
+      __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 w;
@@ -753,18 +710,28 @@ __device__ void softmax_role(const H128Params& p, uint8_t* base, Bars* b, uint32
         w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * f, __uint_as_float(o[8 * q + 3]) * f);
         w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * f, __uint_as_float(o[8 * q + 5]) * f);
         w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * f, __uint_as_float(o[8 * q + 7]) * f);
-        orow[4 * c + q] = w;
+        st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_o, stg, 256 * int(rank) + 128 * wg + 32 * c,
+                     static_cast<int>(tok * 128 + 32 * qd));
+        bulk_commit();
       }
     }
     tc_fence_before();
     mbar_arrive(bar_addr(b->o_free));
-    if (rank == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
+    if (row == 0) SMLA_TL(3, gl, 6);
+    if (rank == 0 && wg == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
   }
+  if (lane == 0) bulk_wait<0>();   // every O block stored before the CTA exits
 }
 
 template <typename IdxT>
 __global__ void __launch_bounds__(kThreads, 1)
-    h128_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const H128Params p) {
+    h128_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                    const H128Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* b = reinterpret_cast<Bars*>(base + kBarOff);
@@ -780,26 +747,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(bar_addr(b->s_full[i]), 1);
-      mbar_init(bar_addr(b->s_comb[i]), kSwapThreads);
-      mbar_init(bar_addr(b->s_free[i]), kSoftmaxThreads);
+      mbar_init(bar_addr(b->s_free[i]), kWgThreads);
     }
+    for (int i = 0; i < 2; ++i)
+      for (int q = 0; q < 4; ++q) mbar_init(bar_addr(b->m_ready[i][q]), 32);
+    mbar_init(bar_addr(b->epi), 2 * kWgThreads);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_addr(b->p_full[i]), kSoftmaxThreads);
+      mbar_init(bar_addr(b->p_full[i]), kWgThreads);
       mbar_init(bar_addr(b->pv_done[i]), 1);
       mbar_init(bar_addr(b->meta_full[i]), 1);
-      mbar_init(bar_addr(b->meta_empty[i]), 1 + kSwapThreads + kSoftmaxThreads);
+      mbar_init(bar_addr(b->meta_empty[i]), 1 + 2 * kWgThreads);
     }
     for (int i = 0; i < kXBufs; ++i) {
       mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
       mbar_init(bar_addr(b->x_free[i]), 4);     // one arrive per peer swap warp
     }
-    mbar_init(bar_addr(b->o_free), kSoftmaxThreads);
+    mbar_init(bar_addr(b->o_free), 2 * kWgThreads);
     mbar_init(bar_addr(b->drain), 1);
     b->abort_flag = 0;
     b->prod_stop = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) prefetch_tmap(&tm_q);
+  if (warp == kScoreWarp0 && lane == 0) prefetch_tmap(&tm_o);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&b->tmem_base), kTmemCols);
     tmem_relinquish();
@@ -815,10 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role(p, base, b, tmem);
     __syncwarp();
-  } else if (warp < kSoftmaxWarp0) {
-    swap_role(p, base, b, tmem, rank, warp, lane);
   } else {
-    softmax_role(p, base, b, tmem, rank, warp, lane);
+    score_role(p, &tm_o, base, b, tmem, rank, warp, lane);
   }
 
   tc_fence_before();
@@ -845,9 +813,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a [rows, 512] row-major matrix, 128-byte swizzle.
+// 2-D bf16 tensor map over a [rows, 512] row-major matrix.
 bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_cols,
-              uint32_t box_rows) {
+              uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
@@ -856,7 +824,7 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_col
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -921,8 +889,9 @@ cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   DeviceState* st = nullptr;
   cudaError_t e = device_state<IdxT>(&st);
   if (e != cudaSuccess) return e;
-  CUtensorMap tq;
-  if (!make_map(&tq, fp.q, static_cast<uint64_t>(fp.T) * 128, 64, 128))
+  CUtensorMap tq, to;
+  if (!make_map(&tq, fp.q, static_cast<uint64_t>(fp.T) * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&to, fp.out, static_cast<uint64_t>(fp.T) * 128, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   unsigned int* err = nullptr;
   if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_h128_error)) != cudaSuccess)
@@ -943,7 +912,7 @@ cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   const int64_t clusters = fp.T < st->max_clusters ? fp.T : st->max_clusters;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(static_cast<unsigned>(2 * clusters), stream, attr);
-  e = cudaLaunchKernelEx(&cfg, h128_fwd_kernel<IdxT>, tq, p);
+  e = cudaLaunchKernelEx(&cfg, h128_fwd_kernel<IdxT>, tq, to, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
