@@ -8,35 +8,38 @@
 // of one SM, and S needs a 512-deep contraction.  Each CTA of the pair owns
 // one 256-wide half of the head dim (rank r: columns 256r..256r+255):
 //   * S_r = Q[:, half r] . K[:, half r]^T, its partial scores over that half;
-//   * the pair swaps partials: each CTA rounds its own partial to fp16, sends
-//     it with st.async (the bytes are counted on the peer's mbarrier, so no
-//     fence per thread is needed) and forms S = f16(S_0) + f16(S_1) in fp32,
-//     which is bit-identical in both CTAs;
+//   * the pair swaps partials: each CTA scales its partial to base-2 logits,
+//     rounds it to fp16, sends it with st.async (the bytes are counted on the
+//     peer's mbarrier, so no fence per thread is needed) and forms
+//     S = f16(S_0) + f16(S_1) in fp32, which is bit-identical in both CTAs;
 //   * both CTAs run the same online softmax on the same S;
 //   * O[:, half r] += P . V[:, half r] into its own TMEM.
-//   TMEM per CTA: O half 256 columns + two 64-column S buffers.
+//   TMEM per CTA: O half 256 columns, three 64-column S buffers, two
+//   32-column P buffers (bf16 pairs, the A operand of P.V).
 //
 // Data movement.  Producer warp 0 compacts the token's valid slots
 // (0 <= idx < num_kv at the index's full width; PR #6002 "Invalid KV rows",
-// "int64 indices") into a row list and loads the token's Q half with 2-D TMA.
-// Producer warps 0-6 gather each tile's 64 half rows (512 B each) with
-// 16-byte cp.async straight into the 128-byte-swizzled layout of a 3-stage
-// ring; each fences its landed copies into the async proxy before it arrives
-// on the stage's barrier.  One tile serves as the K-major B operand of
-// Q.K^T and the MN-major B operand of P.V.  The ragged tail of a token's last
-// tile is zero-filled and its scores are masked: no invalid slot is read.
+// "int64 indices") into a row list one token ahead and loads the token's Q
+// half with 2-D TMA.  Producer warps 0-6 gather each tile's 64 half rows
+// (512 B each) with 16-byte cp.async straight into the 128-byte-swizzled
+// layout of a 3-stage ring; each fences its landed copies into the async
+// proxy before it arrives on the stage's barrier.  One tile serves as the
+// K-major B operand of Q.K^T and the MN-major B operand of P.V.  The ragged
+// tail of a token's last tile is zero-filled and its scores are masked: no
+// invalid slot is read.
 //
-// Pipeline.  The MMA thread issues S(g+1) before P(g).V(g), across token
-// boundaries too; the softmax warps handle tile g-1 while tile g's score swap
-// is in flight.  Softmax is base 2 with the sink folded once in the epilogue
-// (m' = max(m, sink), l' = l 2^(m-m') + 2^(sink-m'), lse = ln2 (m' + log2 l'));
-// the running max is only raised when it grows by more than 2^8, which keeps
-// O rescales rare and is exact because O and l use the same stale max.
+// Pipeline.  The MMA thread issues S and P.V as their inputs arrive, across
+// token boundaries too.  Two score warpgroups take alternate tiles end to end
+// (exchange, combine, softmax, P), handing the running max to each other.
+// Softmax is base 2 with the sink folded once in the epilogue (m' = max(m,
+// sink), l' = l 2^(m-m') + 2^(sink-m'), lse = ln2 (m' + log2 l')); the running
+// max is only raised when it grows by more than 2^8, which keeps O rescales
+// rare and is exact because O and l use the same stale max.  Producer warps
+// 0-3 run each token's epilogue while the score warps start the next token.
 //
 // Warps (512 threads): 0-6 producers, 7 TMEM owner + single-thread MMA issuer,
-// 8-11 score swap with the peer CTA, 12-15 softmax + epilogue (thread = TMEM
-// lane = head in both warpgroups).  Every mbarrier wait is
-// bounded: on expiry the kernel sets an error word, every role leaves its
+// 8-15 two score warpgroups (thread = TMEM lane = head).  Every mbarrier wait
+// is bounded: on expiry the kernel sets an error word, every role leaves its
 // loop, in-flight copies and MMAs are drained, TMEM is freed and the kernel
 // returns.
 #include <cuda.h>
@@ -77,8 +80,8 @@ constexpr uint32_t kStageBytes = kTileN * 256 * 2;    // 32 KB
 constexpr uint32_t kXOff = kKVOff + kStages * kStageBytes;   // peer partials: [2][128][64 fp16]
 constexpr int kXBufs = 2;
 constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
-constexpr uint32_t kStgOff = kXOff + kXBufs * kXBufBytes;    // O store staging: [8 warps][32][32 bf16]
-constexpr uint32_t kStgBytes = 32 * 32 * 2;                  // 2 KB per score warp
+constexpr uint32_t kStgOff = kXOff + kXBufs * kXBufBytes;    // O store staging: [4 warps][2][32][32 bf16]
+constexpr uint32_t kStgBytes = 32 * 32 * 2;                  // 2 KB per block
 constexpr uint32_t kRowsOff = kStgOff + 8 * kStgBytes;       // int32 row lists
 constexpr uint32_t kMaxOff = kRowsOff + 2 * kMaxTopk * 4;    // running max handoff [2][128]
 constexpr uint32_t kSumOff = kMaxOff + 2 * 128 * 4;          // epilogue sums [2][2][2][128]
@@ -93,7 +96,9 @@ struct Bars {
   uint64_t s_full[kSBufs];   // partial S(g) in TMEM (MMA commit)
   uint64_t s_free[kSBufs];   // the score warpgroup has read S(g)
   uint64_t m_ready[2][4];    // running max of tile g published (per tile parity, per quadrant)
-  uint64_t epi;              // both score warpgroups have published their sums
+  uint64_t epi[2];           // both score warpgroups have published their sums (per token
+                             // parity: a warpgroup with no tile in a token may already
+                             // be done with the next one)
   uint64_t p_full[2], pv_done[2];   // per P buffer
   uint64_t x_full[kXBufs], x_free[kXBufs];
   uint64_t o_free;
@@ -214,8 +219,9 @@ __device__ __forceinline__ void land_and_arrive(uint32_t bar) {
 // list, publishes each token's valid count and loads the token's Q half with
 // 2-D TMA.
 template <typename IdxT>
-__device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint8_t* base,
-                              Bars* b, uint32_t rank, int warp, int lane) {
+__device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, const CUtensorMap* tm_o,
+                              uint8_t* base, Bars* b, uint32_t tmem, uint32_t rank, int warp,
+                              int lane) {
   const uint32_t sbase = smem_u32(base);
   int* rows_buf = reinterpret_cast<int*>(base + kRowsOff);   // [2][kMaxTopk]
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
@@ -225,6 +231,76 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
   const bool trace = p.trace != nullptr && rank == 0;
   uint32_t gt = 0, qn = 0, q_loads = 0;
   int it = 0;
+
+  // epilogue state (warps 0-3, warp = TMEM lane quadrant)
+  const bool epi_warp = warp < 4;
+  const int qd = warp & 3;
+  const int row = 32 * qd + lane;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+  const float sk = (epi_warp && p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
+  const float* l_sh = reinterpret_cast<const float*>(base + kSumOff);
+  const uint32_t stg = sbase + kStgOff + qd * 2 * kStgBytes;   // two 2 KB blocks per warp
+  bool ep_pend = false;   // a token whose epilogue has not run yet
+  int64_t ep_tok = 0;
+  uint32_t ep_gl = 0, et = 0;
+  auto epilogue = [&]() -> bool {
+    ep_pend = false;
+    const uint32_t e = et++;
+    // both score warpgroups have published their sums
+    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->epi[e & 1]), (e >> 1) & 1, b, p.err,
+                                                 1u)))
+      return false;
+    const float* lsh = l_sh + (e & 1) * 512;
+    const float l0 = lsh[row], m0 = lsh[128 + row], l1 = lsh[256 + row], m1 = lsh[384 + row];
+    const float m_run = fmaxf(m0, m1);   // the max of the token's last tile
+    const float l_run = l0 * ex2(m0 - m_run) + l1 * ex2(m1 - m_run);
+    // the token's last P.V has completed
+    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[ep_gl & 1]),
+                                                 (ep_gl >> 1) & 1, b, p.err, 1u)))
+      return false;
+    if (lane == 0) SMLA_TL(3, ep_gl, 5);
+    tc_fence_after();
+    float m2 = m_run, l2 = l_run;
+    if (sk != -INFINITY) {
+      m2 = fmaxf(m_run, sk);
+      l2 = l_run * ex2(m_run - m2) + ex2(sk - m2);
+    }
+    const float f = ex2(m_run - m2) / l2;
+    // 32 x 32 bf16 blocks through a double-buffered staging block (64-byte
+    // rows, 64-byte swizzle: 16-byte chunk q of row r at q ^ ((r >> 1) & 3)),
+    // written to global memory by TMA
+#pragma unroll 1
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t o[32];
+      tmem_ld32(tl + 32 * cc, o);
+      tmem_wait_ld();
+      const uint32_t sb = stg + (cc & 1) * kStgBytes;
+      if (lane == 0) bulk_wait_read<1>();   // the block stored two chunks ago has left sb
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * f, __uint_as_float(o[8 * q + 1]) * f);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * f, __uint_as_float(o[8 * q + 3]) * f);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * f, __uint_as_float(o[8 * q + 5]) * f);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * f, __uint_as_float(o[8 * q + 7]) * f);
+        st_shared_v4(sb + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_o, sb, 256 * int(rank) + 32 * cc, static_cast<int>(ep_tok * 128 + 32 * qd));
+        bulk_commit();
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar_addr(b->o_free));
+    if (lane == 0) SMLA_TL(3, ep_gl, 6);
+    if (rank == 0) p.lse[ep_tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
+    return true;
+  };
+  bool run = true;
+
   if (warp == 0 && cid < p.T) {
     const int nv = compact_token<IdxT>(p, cid, rows_buf, trace, lane);
     if (lane == 0) b->prod_nv[0] = nv;
@@ -265,6 +341,13 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         }
       }
     }
+    if (nv == 0 && epi_warp) {   // nothing valid: O = 0; lse = sink (finite) or -inf
+      uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
+                                             256 * rank);
+#pragma unroll
+      for (int cc = 0; cc < 32; ++cc) orow[cc] = make_uint4(0u, 0u, 0u, 0u);
+      if (rank == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
+    }
     const int64_t next = tok + ncl;
     bool compacted = (warp != 0) || (next >= p.T);
     auto compact_next = [&]() {
@@ -279,6 +362,16 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
       for (int j = 0; j < ntiles; ++j) {
         const uint32_t g = gt + j;
         const uint32_t s = g % kStages, ph = (g / kStages) & 1;
+        // this stage is freed by P.V(g - kStages); if that P.V belongs to a
+        // token after the pending one, it waits for O: run the epilogue now
+        if (epi_warp && ep_pend && g >= ep_gl + 1 + kStages) {
+          if (pending >= 0) {
+            cp_async_wait<0>();
+            land_and_arrive(bar_addr(b->kv_full[pending]));
+            pending = -1;
+          }
+          if (!(run = epilogue())) break;
+        }
         // Overlap the previous tile's copies with this issue only if this
         // stage is already free; otherwise count them first, so a tile's
         // readiness never waits on a later stage.
@@ -322,9 +415,19 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, uint
         if (lane == 0) SMLA_TL(0, gt + ntiles - 1, 2);
       }
       gt += ntiles;
+      if (epi_warp && run) {   // epilogues run in token order
+        if (ep_pend) run = epilogue();
+        ep_pend = true;
+        ep_tok = tok;
+        ep_gl = gt - 1;
+      }
     }
     if (!compacted) compact_next();
+    // after a failed epilogue (the abort flag is set) every producer warp leaves
+    // together at the next token's start, never from here
   }
+  if (epi_warp && run && ep_pend) epilogue();
+  if (epi_warp && lane == 0) bulk_wait<0>();   // every O block stored before the CTA exits
   cp_async_wait<0>();   // drain: no copy of ours may land after the CTA exits
   if (warp == 0 && lane == 0 && q_loads > 0)
     wait_bar<false, true>(bar_addr(b->q_full), (q_loads - 1) & 1, b, p.err, 1u);
@@ -477,8 +580,8 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
 // Each warpgroup keeps the sum l of its own tiles (relative to the max it last
 // saw); at the end of a token the two sums are merged through shared memory
 // and the warpgroups normalise and store one half each of this CTA's O half.
-__device__ void score_role(const H128Params& p, const CUtensorMap* tm_o, uint8_t* base, Bars* b,
-                           uint32_t tmem, uint32_t rank, int warp, int lane) {
+__device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
+                           uint32_t rank, int warp, int lane) {
   const uint32_t sbase = smem_u32(base);
   const int wg = (warp - kScoreWarp0) >> 2;   // 0 or 1
   const int qd = warp & 3;                    // TMEM lane quadrant
@@ -487,10 +590,8 @@ __device__ void score_role(const H128Params& p, const CUtensorMap* tm_o, uint8_t
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   const uint32_t peer = rank ^ 1u;
   const float sl2 = p.scale * kLog2e;
-  const float sk = (p.sink != nullptr) ? p.sink[row] * kLog2e : -INFINITY;
   float* m_sh = reinterpret_cast<float*>(base + kMaxOff);   // [2 tile parities][128]
   float* l_sh = reinterpret_cast<float*>(base + kSumOff);   // [2 tokens][2 wg][2 (l, m)][128]
-  const uint32_t stg = sbase + kStgOff + (warp - kScoreWarp0) * kStgBytes;
   uint32_t recv_local[kXBufs], recv_peer[kXBufs], xfull_peer[kXBufs], xfree_peer[kXBufs];
 #pragma unroll
   for (int i = 0; i < kXBufs; ++i) {
@@ -510,15 +611,7 @@ __device__ void score_role(const H128Params& p, const CUtensorMap* tm_o, uint8_t
     if (!ok) break;
     const int nv = b->nvalid[slot];
     mbar_arrive(bar_addr(b->meta_empty[slot]));
-    // this warpgroup's 128 columns of the CTA's 256-column O half (empty tokens only)
-    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * 128 + row) * int64_t(kHeadDim) +
-                                           256 * rank + 128 * wg);
-    if (nv == 0) {   // nothing valid: O = 0; lse = sink (finite) or -inf
-#pragma unroll
-      for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-      if (rank == 0 && wg == 0) p.lse[tok * 128 + row] = (sk != -INFINITY) ? sk * kLn2 : -INFINITY;
-      continue;
-    }
+    if (nv == 0) continue;   // written by the producer warps
     const int ntiles = (nv + kTileN - 1) / kTileN;
     float l_w = 0.f, m_lw = -INFINITY;   // this warpgroup's sum and the max it is relative to
     for (int j = 0; j < ntiles; ++j) {
@@ -669,63 +762,13 @@ __device__ void score_role(const H128Params& p, const CUtensorMap* tm_o, uint8_t
     }
     if (!ok) break;
     gt += ntiles;
-    // epilogue: merge the two warpgroups' sums, wait for the token's last P.V,
-    // fold the sink, normalise, store this warpgroup's 128 columns
+    // publish this warpgroup's sum for the token's epilogue (run by producer warps 0-3)
     float* lsh = l_sh + (et & 1) * 512;
     lsh[wg * 256 + row] = l_w;
     lsh[wg * 256 + 128 + row] = m_lw;
-    mbar_arrive(bar_addr(b->epi));
-    if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->epi), et & 1, b, p.err, 4u))))
-      break;
-    const float l_o = lsh[(wg ^ 1) * 256 + row], m_o = lsh[(wg ^ 1) * 256 + 128 + row];
+    mbar_arrive(bar_addr(b->epi[et & 1]));
     ++et;
-    const float m_run = fmaxf(m_lw, m_o);   // the max of the token's last tile
-    const float l_run = l_w * ex2(m_lw - m_run) + l_o * ex2(m_o - m_run);
-    const uint32_t gl = gt - 1;
-    if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[gl & 1]),
-                                                       (gl >> 1) & 1, b, p.err, 4u))))
-      break;
-    if (row == 0) SMLA_TL(3, gl, 5);
-    tc_fence_after();
-    float m2 = m_run, l2 = l_run;
-    if (sk != -INFINITY) {
-      m2 = fmaxf(m_run, sk);
-      l2 = l_run * ex2(m_run - m2) + ex2(sk - m2);
-    }
-    const float f = ex2(m_run - m2) / l2;
-    // 32 x 32 bf16 blocks through this warp's staging buffer (64-byte rows,
-    // 64-byte swizzle: 16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3)),
-    // written to global memory by TMA (whole lines instead of 32 rows per store)
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[32];
-      tmem_ld32(tl + 128 * wg + 32 * c, o);
-      tmem_wait_ld();
-      if (lane == 0) bulk_wait_read<0>();   // the previous block has left the buffer
-      __syncwarp();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * f, __uint_as_float(o[8 * q + 1]) * f);
-        w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * f, __uint_as_float(o[8 * q + 3]) * f);
-        w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * f, __uint_as_float(o[8 * q + 5]) * f);
-        w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * f, __uint_as_float(o[8 * q + 7]) * f);
-        st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(tm_o, stg, 256 * int(rank) + 128 * wg + 32 * c,
-                     static_cast<int>(tok * 128 + 32 * qd));
-        bulk_commit();
-      }
-    }
-    tc_fence_before();
-    mbar_arrive(bar_addr(b->o_free));
-    if (row == 0) SMLA_TL(3, gl, 6);
-    if (rank == 0 && wg == 0) p.lse[tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
   }
-  if (lane == 0) bulk_wait<0>();   // every O block stored before the CTA exits
 }
 
 template <typename IdxT>
@@ -751,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i)
       for (int q = 0; q < 4; ++q) mbar_init(bar_addr(b->m_ready[i][q]), 32);
-    mbar_init(bar_addr(b->epi), 2 * kWgThreads);
+    for (int i = 0; i < 2; ++i) mbar_init(bar_addr(b->epi[i]), 2 * kWgThreads);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->p_full[i]), kWgThreads);
       mbar_init(bar_addr(b->pv_done[i]), 1);
@@ -762,14 +805,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
       mbar_init(bar_addr(b->x_free[i]), 4);     // one arrive per peer swap warp
     }
-    mbar_init(bar_addr(b->o_free), 2 * kWgThreads);
+    mbar_init(bar_addr(b->o_free), 128);   // producer warps 0-3 after the epilogue
     mbar_init(bar_addr(b->drain), 1);
     b->abort_flag = 0;
     b->prod_stop = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) prefetch_tmap(&tm_q);
-  if (warp == kScoreWarp0 && lane == 0) prefetch_tmap(&tm_o);
+  if (warp == 1 && lane == 0) prefetch_tmap(&tm_o);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&b->tmem_base), kTmemCols);
     tmem_relinquish();
@@ -781,12 +824,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = b->tmem_base;
 
   if (warp < kMmaWarp) {
-    producer_role<IdxT>(p, &tm_q, base, b, rank, warp, lane);
+    producer_role<IdxT>(p, &tm_q, &tm_o, base, b, tmem, rank, warp, lane);
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role(p, base, b, tmem);
     __syncwarp();
   } else {
-    score_role(p, &tm_o, base, b, tmem, rank, warp, lane);
+    score_role(p, base, b, tmem, rank, warp, lane);
   }
 
   tc_fence_before();
