@@ -243,7 +243,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
   bool ep_pend = false;   // a token whose epilogue has not run yet
   int64_t ep_tok = 0;
   uint32_t ep_gl = 0, et = 0;
-  auto epilogue = [&]() -> bool {
+  auto epilogue = [&](auto&& mid) -> bool {
     ep_pend = false;
     const uint32_t e = et++;
     // both score warpgroups have published their sums
@@ -268,33 +268,47 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
     const float f = ex2(m_run - m2) / l2;
     // 32 x 32 bf16 blocks through a double-buffered staging block (64-byte
     // rows, 64-byte swizzle: 16-byte chunk q of row r at q ^ ((r >> 1) & 3)),
-    // written to global memory by TMA
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      uint32_t o[32];
-      tmem_ld32(tl + 32 * cc, o);
-      tmem_wait_ld();
-      const uint32_t sb = stg + (cc & 1) * kStgBytes;
-      if (lane == 0) bulk_wait_read<1>();   // the block stored two chunks ago has left sb
+    // written to global memory by TMA.  O is released as soon as all of it has
+    // been read from TMEM: the first kHeld blocks wait in registers (packed
+    // bf16) while the others go through the staging blocks.
+    constexpr int kHeld = 3;
+    uint32_t held[kHeld][16];
+    auto put = [&](int cc, const uint32_t* w16, int slot) {   // one block: staging -> TMA
+      const uint32_t sb = stg + (slot & 1) * kStgBytes;
+      if (lane == 0) bulk_wait_read<1>();   // the block stored two slots ago has left sb
       __syncwarp();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * f, __uint_as_float(o[8 * q + 1]) * f);
-        w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * f, __uint_as_float(o[8 * q + 3]) * f);
-        w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * f, __uint_as_float(o[8 * q + 5]) * f);
-        w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * f, __uint_as_float(o[8 * q + 7]) * f);
-        st_shared_v4(sb + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
-      }
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(sb + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4),
+                     make_uint4(w16[4 * q], w16[4 * q + 1], w16[4 * q + 2], w16[4 * q + 3]));
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         tma_store_2d(tm_o, sb, 256 * int(rank) + 32 * cc, static_cast<int>(ep_tok * 128 + 32 * qd));
         bulk_commit();
       }
+    };
+    auto load = [&](int cc, uint32_t* w16) {   // one block: TMEM -> normalised bf16 pairs
+      uint32_t o[32];
+      tmem_ld32(tl + 32 * cc, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w16[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+    };
+#pragma unroll
+    for (int cc = 0; cc < kHeld; ++cc) load(cc, held[cc]);
+#pragma unroll 1
+    for (int cc = kHeld; cc < 8; ++cc) {
+      uint32_t w16[16];
+      load(cc, w16);
+      put(cc, w16, cc - kHeld);
+      if (cc == kHeld) mid();
     }
     tc_fence_before();
-    mbar_arrive(bar_addr(b->o_free));
+    mbar_arrive(bar_addr(b->o_free));   // all of O has been read
+#pragma unroll
+    for (int cc = 0; cc < kHeld; ++cc) put(cc, held[cc], 8 - kHeld + cc);
     if (lane == 0) SMLA_TL(3, ep_gl, 6);
     if (rank == 0) p.lse[ep_tok * 128 + row] = (m2 + log2f(l2)) * kLn2;
     return true;
@@ -370,7 +384,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
             land_and_arrive(bar_addr(b->kv_full[pending]));
             pending = -1;
           }
-          if (!(run = epilogue())) break;
+          if (!(run = epilogue([]() {}))) break;
         }
         // Overlap the previous tile's copies with this issue only if this
         // stage is already free; otherwise count them first, so a tile's
@@ -408,6 +422,16 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
           if (lane == 0) SMLA_TL(0, g - 1, 2);
         }
         pending = static_cast<int>(s);
+        // this tile's stage was freed by the pending token's last P.V: run its
+        // epilogue now (counting this tile's copies once they have landed, mid-way)
+        if (epi_warp && ep_pend && g >= ep_gl + kStages) {
+          if (!(run = epilogue([&]() {
+                cp_async_wait<0>();
+                land_and_arrive(bar_addr(b->kv_full[pending]));
+                pending = -1;
+              })))
+            break;
+        }
       }
       if (pending >= 0) {
         cp_async_wait<0>();
@@ -416,7 +440,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
       }
       gt += ntiles;
       if (epi_warp && run) {   // epilogues run in token order
-        if (ep_pend) run = epilogue();
+        if (ep_pend) run = epilogue([]() {});
         ep_pend = true;
         ep_tok = tok;
         ep_gl = gt - 1;
@@ -426,7 +450,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
     // after a failed epilogue (the abort flag is set) every producer warp leaves
     // together at the next token's start, never from here
   }
-  if (epi_warp && run && ep_pend) epilogue();
+  if (epi_warp && run && ep_pend) epilogue([]() {});
   if (epi_warp && lane == 0) bulk_wait<0>();   // every O block stored before the CTA exits
   cp_async_wait<0>();   // drain: no copy of ours may land after the CTA exits
   if (warp == 0 && lane == 0 && q_loads > 0)
