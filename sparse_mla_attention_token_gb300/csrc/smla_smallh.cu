@@ -39,15 +39,18 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kBN = 64;           // gathered rows per tile
 constexpr int kHG = 16;           // heads per CTA (mma M)
-constexpr int kSredStride = 72;   // floats per row of a warp's partial scores (bank spread)
-constexpr int kPStride = 72;      // bf16 per row of P (bank spread for ldmatrix)
 constexpr int kOStride = 520;     // bf16 per row of the staged output tile (bank spread)
 constexpr int kRowBytes = kHeadDim * 2;
 
+// kBN gathered rows per tile: 64, or 32 when a CTA's slot range holds at most
+// 32 slots (no padded MMA work; half the shared memory and at most 128
+// registers, so two CTAs share an SM and hide each other's gather latency).
+template <int kBN>
 struct __align__(128) Smem {
-  __nv_bfloat16 kv[2][kBN * kHeadDim];     // 2 x 64 KB; 16 B chunk c of row r at c ^ (r & 7)
+  static constexpr int kSredStride = kBN + 8;   // floats per row of a warp's partial scores
+  static constexpr int kPStride = kBN + 8;      // bf16 per row of P (bank spread for ldmatrix)
+  __nv_bfloat16 kv[2][kBN * kHeadDim];     // 2 stages; 16 B chunk c of row r at c ^ (r & 7)
   float sred[kWarps][kHG * kSredStride];   // per-warp partial scores
   __nv_bfloat16 p[kHG * kPStride];         // probabilities, A operand of P.V
   float alpha[kHG];                        // per-row rescale of O for the current tile
@@ -56,15 +59,20 @@ struct __align__(128) Smem {
   int rows[kSmallHMaxSlots];               // compacted valid kv rows, slot order
   int warp_cnt[kWarps];
 };
+static_assert(sizeof(Smem<32>::kv[0]) >= kHG * kOStride * 2, "output staging fits one stage");
 
 __device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t base, int r, int c) {
   return base + r * kRowBytes + ((c ^ (r & 7)) << 4);
 }
 
-template <typename IdxT, bool kSplit>
-__global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams p) {
+template <typename IdxT, bool kSplit, int kBN>
+__global__ void __launch_bounds__(kThreads, kBN == 32 ? 2 : 1) smallh_fwd_kernel(const FwdParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  using SmemT = Smem<kBN>;
+  constexpr int kSredStride = SmemT::kSredStride, kPStride = SmemT::kPStride;
+  constexpr int kNT = kBN / 8;     // 8-slot n-tiles of S
+  constexpr int kCols = kBN / 16;  // softmax columns per lane (16 lanes per row)
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -143,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams
   const int ntiles = (nvalid + kBN - 1) / kBN;
   const float sl2 = p.scale * kLog2e;
   const int srow = 2 * warp + (lane >> 4);   // softmax row owned by this half-warp
-  const int sc0 = (lane & 15) * 4;           // its 4 columns
+  const int sc0 = (lane & 15) * kCols;       // its kCols columns
   float m_run = -INFINITY, l_run = 0.f;
   float acc[8][4];
 #pragma unroll
@@ -158,14 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams
     const uint32_t kvs = smem_u32(sm.kv[stage]);
 
     // ---- 3. partial S over this warp's 64 columns
-    float s[8][4];
+    float s[kNT][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+    for (int i = 0; i < kNT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
 #pragma unroll
     for (int kp = 0; kp < 2; ++kp) {
       const int c = warp * 8 + kp * 4 + (lane >> 3);
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < kNT; ++nt) {
         const int r = nt * 8 + (lane & 7);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(kv_chunk_addr(kvs, r, c), b0, b1, b2, b3);
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams
     }
     float* sw = sm.sred[warp];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < kNT; ++nt) {
       *reinterpret_cast<float2*>(&sw[g * kSredStride + nt * 8 + 2 * tig]) =
           make_float2(s[nt][0], s[nt][1]);
       *reinterpret_cast<float2*>(&sw[(g + 8) * kSredStride + nt * 8 + 2 * tig]) =
@@ -185,33 +193,45 @@ __global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams
 
     // ---- 4. reduce the 8 partials, online softmax (base 2)
     {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      float a[kCols];
+#pragma unroll
+      for (int k = 0; k < kCols; ++k) a[k] = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float4 v = *reinterpret_cast<const float4*>(&sm.sred[w][srow * kSredStride + sc0]);
-        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        const float* src = &sm.sred[w][srow * kSredStride + sc0];
+        if constexpr (kCols == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          a[0] += v.x; a[1] += v.y; a[2] += v.z; a[3] += v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          a[0] += v.x; a[1] += v.y;
+        }
       }
       const int col = it * kBN + sc0;
-      float x0 = (col + 0 < nvalid) ? a.x * sl2 : -INFINITY;
-      float x1 = (col + 1 < nvalid) ? a.y * sl2 : -INFINITY;
-      float x2 = (col + 2 < nvalid) ? a.z * sl2 : -INFINITY;
-      float x3 = (col + 3 < nvalid) ? a.w * sl2 : -INFINITY;
-      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      float x[kCols];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kCols; ++k) {
+        x[k] = (col + k < nvalid) ? a[k] * sl2 : -INFINITY;
+        mx = fmaxf(mx, x[k]);
+      }
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float m_new = fmaxf(m_run, mx);  // finite: the tile holds >= 1 valid row
       const float alpha = ex2(m_run - m_new);
-      const float e0 = ex2(x0 - m_new), e1 = ex2(x1 - m_new);
-      const float e2 = ex2(x2 - m_new), e3 = ex2(x3 - m_new);
-      float ps = (e0 + e1) + (e2 + e3);
+      float ps = 0.f;
+#pragma unroll
+      for (int k = 0; k < kCols; ++k) {
+        x[k] = ex2(x[k] - m_new);
+        ps += x[k];
+      }
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
       l_run = l_run * alpha + ps;
       m_run = m_new;
-      uint2 pk;
-      pk.x = pack_bf16x2(e0, e1);
-      pk.y = pack_bf16x2(e2, e3);
-      *reinterpret_cast<uint2*>(&sm.p[srow * kPStride + sc0]) = pk;
+#pragma unroll
+      for (int k = 0; k < kCols; k += 2)
+        *reinterpret_cast<uint32_t*>(&sm.p[srow * kPStride + sc0 + k]) = pack_bf16x2(x[k], x[k + 1]);
       if ((lane & 15) == 0) sm.alpha[srow] = alpha;
     }
     __syncthreads();
@@ -226,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams
       }
       const uint32_t ps = smem_u32(sm.p);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
+      for (int ks = 0; ks < kBN / 16; ++ks) {
         uint32_t pa[4];
         const int pr = ((lane >> 3) & 1) * 8 + (lane & 7);
         const int pc = ks * 16 + (lane >> 4) * 8;
@@ -301,10 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1) smallh_fwd_kernel(const FwdParams
   }
 }
 
-template <typename IdxT, bool kSplit>
-cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
-  auto kern = smallh_fwd_kernel<IdxT, kSplit>;
-  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+// slots a CTA covers: its share of the index list
+int slots_per_cta(const FwdParams& p) { return (p.topk + p.splits - 1) / p.splits; }
+
+template <typename IdxT, bool kSplit, int kBN>
+cudaError_t launch_bn(const FwdParams& p, cudaStream_t stream) {
+  auto kern = smallh_fwd_kernel<IdxT, kSplit, kBN>;
+  const int smem = static_cast<int>(sizeof(Smem<kBN>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>((p.H + kHG - 1) / kHG),
@@ -313,13 +336,20 @@ cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <typename IdxT, bool kSplit>
+cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
+  return slots_per_cta(p) <= 32 ? launch_bn<IdxT, kSplit, 32>(p, stream)
+                                : launch_bn<IdxT, kSplit, 64>(p, stream);
+}
+
 }  // namespace
 
-int smallh_geometry(int64_t T, int32_t H, int32_t splits, LaunchGeom* g) {
+int smallh_geometry(int64_t T, int32_t H, int32_t topk, int32_t splits, LaunchGeom* g) {
   g->grid_ctas = static_cast<int>(T * ((H + kHG - 1) / kHG) * splits);
   g->threads = kThreads;
   g->cluster = 1;
-  g->smem = static_cast<int>(sizeof(Smem)) + 1024;
+  g->smem = static_cast<int>((topk + splits - 1) / splits <= 32 ? sizeof(Smem<32>) : sizeof(Smem<64>)) +
+            1024;
   return 0;
 }
 
