@@ -248,7 +248,7 @@ smla_status_t sparse_mla_launch_config(int64_t T, int32_t H, int32_t topk, int64
   if (st != SMLA_OK) return st;
   smla::LaunchGeom g{0, 0, 0, 0};
   const int e = pl.family == 1 ? smla::h128_geometry(T, &g)
-                               : smla::smallh_geometry(T, H, topk, pl.splits, &g);
+                               : smla::smallh_geometry(T, H, pl.splits, &g);
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "launch geometry");
   if (grid_ctas) *grid_ctas = g.grid_ctas;
   if (cta_threads) *cta_threads = g.threads;

@@ -56,7 +56,7 @@ struct LaunchGeom {
   int cluster;
   int smem;
 };
-int smallh_geometry(int64_t T, int32_t H, int32_t topk, int32_t splits, LaunchGeom* g);
+int smallh_geometry(int64_t T, int32_t H, int32_t splits, LaunchGeom* g);
 int h128_geometry(int64_t T, LaunchGeom* g);
 
 // Partial rows (splits * T * H) the static scratch of the allocation-free

@@ -12,7 +12,7 @@
 //     (0 <= idx < num_kv; int64 never narrowed before the check) and the valid
 //     rows are compacted, in slot order, into a shared-memory row list;
 //     invalid slots are never read (PR #6002 "Invalid KV rows");
-//   * rows are gathered 64 per tile with 16-byte cp.async into a two-stage
+//   * rows are gathered 32 per tile with 16-byte cp.async into a two-stage
 //     ring (the next tile lands while this one is computed); the ragged tail
 //     of the last tile is zero-filled, so no pad row can inject NaN;
 //   * M = 16 heads is below tcgen05's smallest tile (M = 64), so the two
@@ -43,10 +43,10 @@ constexpr int kHG = 16;           // heads per CTA (mma M)
 constexpr int kOStride = 520;     // bf16 per row of the staged output tile (bank spread)
 constexpr int kRowBytes = kHeadDim * 2;
 
-// kBN gathered rows per tile: 64, or 32 when a CTA's slot range holds at most
-// 32 slots (no padded MMA work; half the shared memory and at most 128
-// registers, so two CTAs share an SM and hide each other's gather latency).
-template <int kBN>
+// 32 gathered rows per tile: ~95 KB of shared memory and at most 128
+// registers, so two CTAs share an SM and hide each other's gather latency
+// (measured faster than 64-row tiles at one CTA per SM for every slot count).
+constexpr int kBN = 32;
 struct __align__(128) Smem {
   static constexpr int kSredStride = kBN + 8;   // floats per row of a warp's partial scores
   static constexpr int kPStride = kBN + 8;      // bf16 per row of P (bank spread for ldmatrix)
@@ -59,16 +59,16 @@ struct __align__(128) Smem {
   int rows[kSmallHMaxSlots];               // compacted valid kv rows, slot order
   int warp_cnt[kWarps];
 };
-static_assert(sizeof(Smem<32>::kv[0]) >= kHG * kOStride * 2, "output staging fits one stage");
+static_assert(sizeof(Smem::kv[0]) >= kHG * kOStride * 2, "output staging fits one stage");
 
 __device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t base, int r, int c) {
   return base + r * kRowBytes + ((c ^ (r & 7)) << 4);
 }
 
-template <typename IdxT, bool kSplit, int kBN>
-__global__ void __launch_bounds__(kThreads, kBN == 32 ? 2 : 1) smallh_fwd_kernel(const FwdParams p) {
+template <typename IdxT, bool kSplit>
+__global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  using SmemT = Smem<kBN>;
+  using SmemT = Smem;
   constexpr int kSredStride = SmemT::kSredStride, kPStride = SmemT::kPStride;
   constexpr int kNT = kBN / 8;     // 8-slot n-tiles of S
   constexpr int kCols = kBN / 16;  // softmax columns per lane (16 lanes per row)
@@ -321,13 +321,10 @@ __global__ void __launch_bounds__(kThreads, kBN == 32 ? 2 : 1) smallh_fwd_kernel
   }
 }
 
-// slots a CTA covers: its share of the index list
-int slots_per_cta(const FwdParams& p) { return (p.topk + p.splits - 1) / p.splits; }
-
-template <typename IdxT, bool kSplit, int kBN>
-cudaError_t launch_bn(const FwdParams& p, cudaStream_t stream) {
-  auto kern = smallh_fwd_kernel<IdxT, kSplit, kBN>;
-  const int smem = static_cast<int>(sizeof(Smem<kBN>)) + 1024;
+template <typename IdxT, bool kSplit>
+cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
+  auto kern = smallh_fwd_kernel<IdxT, kSplit>;
+  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>((p.H + kHG - 1) / kHG),
@@ -336,20 +333,13 @@ cudaError_t launch_bn(const FwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <typename IdxT, bool kSplit>
-cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
-  return slots_per_cta(p) <= 32 ? launch_bn<IdxT, kSplit, 32>(p, stream)
-                                : launch_bn<IdxT, kSplit, 64>(p, stream);
-}
-
 }  // namespace
 
-int smallh_geometry(int64_t T, int32_t H, int32_t topk, int32_t splits, LaunchGeom* g) {
+int smallh_geometry(int64_t T, int32_t H, int32_t splits, LaunchGeom* g) {
   g->grid_ctas = static_cast<int>(T * ((H + kHG - 1) / kHG) * splits);
   g->threads = kThreads;
   g->cluster = 1;
-  g->smem = static_cast<int>((topk + splits - 1) / splits <= 32 ? sizeof(Smem<32>) : sizeof(Smem<64>)) +
-            1024;
+  g->smem = static_cast<int>(sizeof(Smem)) + 1024;
   return 0;
 }
 
