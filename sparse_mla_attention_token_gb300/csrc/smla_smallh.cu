@@ -91,7 +91,24 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
   const int j1 = min(p.topk, j0 + chunk);
   const IdxT* idx = static_cast<const IdxT*>(p.idx) + t * p.topk;
 
-  // ---- 1. classify every slot at full width, compact the valid rows (slot order)
+  // ---- 1. this warp's Q fragments: rows = heads of the group, k = its 64 columns
+  //      (issued first: their latency overlaps the index list's)
+  uint32_t qa[4][4];
+  {
+    const uint32_t* q32 = static_cast<const uint32_t*>(p.q);
+    const int64_t rbase = (t * H + h0) * kHeadDim;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int d = warp * 64 + kk * 16 + 2 * tig;
+      const bool lo = g < hvalid, hi = (g + 8) < hvalid;
+      qa[kk][0] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d) >> 1] : 0u;
+      qa[kk][1] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d) >> 1] : 0u;
+      qa[kk][2] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d + 8) >> 1] : 0u;
+      qa[kk][3] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d + 8) >> 1] : 0u;
+    }
+  }
+
+  // ---- 2. classify every slot at full width, compact the valid rows (slot order)
   int nvalid = 0;
   for (int base = j0; base < j1; base += kThreads) {
     const int j = base + tid;
@@ -116,22 +133,6 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
     if (v) sm.rows[off + __popc(ball & ((1u << lane) - 1u))] = row;
     nvalid += total;
     __syncthreads();
-  }
-
-  // ---- 2. this warp's Q fragments: rows = heads of the group, k = its 64 columns
-  uint32_t qa[4][4];
-  {
-    const uint32_t* q32 = static_cast<const uint32_t*>(p.q);
-    const int64_t rbase = (t * H + h0) * kHeadDim;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const int d = warp * 64 + kk * 16 + 2 * tig;
-      const bool lo = g < hvalid, hi = (g + 8) < hvalid;
-      qa[kk][0] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d) >> 1] : 0u;
-      qa[kk][1] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d) >> 1] : 0u;
-      qa[kk][2] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d + 8) >> 1] : 0u;
-      qa[kk][3] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d + 8) >> 1] : 0u;
-    }
   }
 
   const char* kvb = static_cast<const char*>(p.kv);
