@@ -55,7 +55,9 @@ typedef enum {
   SMLA_ERR_CUDA = 8,             /* a CUDA runtime call failed (see _last_cuda_error)*/
   SMLA_ERR_DEVICE_TIMEOUT = 9,   /* a kernel's bounded wait expired (device status)  */
   SMLA_ERR_BAD_SPLITS = 10,      /* forced split count out of range                  */
-  SMLA_ERR_SCRATCH_LIMIT = 11    /* splits*T*H beyond the library's static scratch   */
+  SMLA_ERR_SCRATCH_LIMIT = 11,   /* splits*T*H beyond the library's static scratch   */
+  SMLA_ERR_WORKSPACE = 12        /* host-buffer call: workspace NULL, short or       */
+                                 /* not 256-byte aligned                             */
 } smla_status_t;
 
 /*
@@ -134,6 +136,51 @@ smla_status_t sparse_mla_fwd_static_scratch(const void* q, const void* kv,
                                             const float* attn_sink, float scale, void* out,
                                             float* lse, int64_t T, int32_t H, int64_t num_kv,
                                             int32_t topk, void* stream, int32_t num_splits);
+
+/*
+ * sparse_mla_fwd_host -- the forward on HOST buffers: copies the inputs in,
+ * runs sparse_mla_fwd and copies O and lse out, overlapping the copies with
+ * the computation.
+ *
+ * The pages have no counterpart to this entry point; it is the call for a
+ * caller whose tensors live in host memory (the end-to-end path).  Tokens are
+ * independent, so the call splits them into chunks and pipelines them on two
+ * copy streams of its own: while chunk c is computed, chunk c+1's q and index
+ * rows are copied in and chunk c-1's O and lse copied out.  kv (and the sink)
+ * go in first, whole: any token may read any kv row.  Every chunk runs with
+ * the kernel and split count sparse_mla_fwd would pick for the whole call, so
+ * the results are bit-identical to sparse_mla_fwd's on the same inputs.
+ *
+ *   q_host, kv_host, topk_indices_host, attn_sink_host (or NULL), out_host,
+ *   lse_host     HOST pointers, the layouts of sparse_mla_fwd.  For the copies
+ *                to overlap they must be page-locked (cudaHostAlloc or
+ *                cudaHostRegister); pageable memory works but serialises.
+ *   workspace    DEVICE memory of at least sparse_mla_fwd_host_workspace()
+ *                bytes, 256-byte aligned, owned by the caller and not touched
+ *                by other work until `stream` has passed this call; the call
+ *                allocates nothing.
+ *   stream       the call is ordered on it: its copies start after the
+ *                stream's earlier work, and the stream waits for the last
+ *                copy out, so out_host / lse_host hold the results once
+ *                `stream` has passed the call.
+ *   Errors       as sparse_mla_fwd (same host checks on the host pointers),
+ *                plus SMLA_ERR_WORKSPACE; all before any CUDA call.
+ */
+smla_status_t sparse_mla_fwd_host(const void* q_host, const void* kv_host,
+                                  const void* topk_indices_host, int32_t index_dtype,
+                                  const float* attn_sink_host, float scale, void* out_host,
+                                  float* lse_host, int64_t T, int32_t H, int64_t num_kv,
+                                  int32_t topk, void* workspace, uint64_t workspace_bytes,
+                                  void* stream);
+
+/*
+ * sparse_mla_fwd_host_workspace -- device workspace bytes sparse_mla_fwd_host
+ * needs for these sizes (host only, no CUDA call): room for kv, q, the index
+ * rows, the sink, O and lse, each 256-byte aligned.  has_sink: 0 or 1.
+ */
+smla_status_t sparse_mla_fwd_host_workspace(int64_t T, int32_t H, int32_t topk, int64_t num_kv,
+                                            int32_t index_dtype, int32_t has_sink,
+                                            uint64_t* bytes);
 
 /*
  * sparse_mla_plan -- what sparse_mla_fwd_ex would launch, without launching.

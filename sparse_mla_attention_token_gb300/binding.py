@@ -28,16 +28,19 @@ STATUS = {
     0: "SMLA_OK", 1: "SMLA_ERR_NULL_PTR", 2: "SMLA_ERR_BAD_SHAPE", 3: "SMLA_ERR_UNSUPPORTED_H",
     4: "SMLA_ERR_BAD_INDEX_DTYPE", 5: "SMLA_ERR_MISALIGNED", 6: "SMLA_ERR_BAD_SCALE",
     7: "SMLA_ERR_ALIASING", 8: "SMLA_ERR_CUDA", 9: "SMLA_ERR_DEVICE_TIMEOUT",
-    10: "SMLA_ERR_BAD_SPLITS", 11: "SMLA_ERR_SCRATCH_LIMIT",
+    10: "SMLA_ERR_BAD_SPLITS", 11: "SMLA_ERR_SCRATCH_LIMIT", 12: "SMLA_ERR_WORKSPACE",
 }
 
 # exported symbol -> (restype, argtypes)
 _P, _I32, _I64, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+_U64 = ctypes.c_uint64
 _FWD_ARGS = [_P, _P, _P, _I32, _P, _F32, _P, _P, _I64, _I32, _I64, _I32, _P]
 SIGNATURES = {
     "sparse_mla_fwd": (_I32, _FWD_ARGS),
     "sparse_mla_fwd_ex": (_I32, _FWD_ARGS + [_I32, _P]),
     "sparse_mla_fwd_static_scratch": (_I32, _FWD_ARGS + [_I32]),
+    "sparse_mla_fwd_host": (_I32, _FWD_ARGS[:-1] + [_P, _U64, _P]),
+    "sparse_mla_fwd_host_workspace": (_I32, [_I64, _I32, _I32, _I64, _I32, _I32, _P]),
     "sparse_mla_plan": (_I32, [_I64, _I32, _I32, _I32, _P, _P, _P]),
     "sparse_mla_launch_config": (_I32, [_I64, _I32, _I32, _I64, _I32, _P, _P, _P, _P]),
     "sparse_mla_device_status": (_I32, [_P]),
@@ -252,4 +255,61 @@ def sparse_mla_fwd_static_scratch(q, kv, topk_indices, out, lse, attn_sink=None,
             _stream_ptr(stream), int(num_splits))
     if st != SMLA_OK:
         raise SparseMLAError(st, "sparse_mla_fwd_static_scratch")
+    return out, lse
+
+
+def sparse_mla_fwd_host_workspace(T: int, H: int, topk: int, num_kv: int,
+                                  index_dtype: int = SMLA_IDX_INT32, has_sink: bool = True) -> int:
+    """Device workspace bytes of :func:`sparse_mla_fwd_host` for these sizes."""
+    n = ctypes.c_uint64(0)
+    st = lib().sparse_mla_fwd_host_workspace(int(T), int(H), int(topk), int(num_kv),
+                                             int(index_dtype), 1 if has_sink else 0, ctypes.byref(n))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_fwd_host_workspace")
+    return int(n.value)
+
+
+def sparse_mla_fwd_host(q, kv, topk_indices, out, lse, attn_sink=None, workspace=None,
+                        scale: Optional[float] = None, stream=None):
+    """The forward on HOST tensors (copies in, compute, copies out, overlapped).
+
+    ``q``, ``kv``, ``topk_indices``, ``attn_sink`` (or None), ``out`` and
+    ``lse`` are CPU tensors, best page-locked (``pin_memory()``) so that the
+    copies overlap; ``workspace`` is a CUDA uint8 tensor of at least
+    :func:`sparse_mla_fwd_host_workspace` bytes on the current device.  The
+    results are in ``out`` / ``lse`` once ``stream`` (default: the current
+    stream) has passed the call.  Returns ``(out, lse)``.
+    """
+    import torch
+    if q.dtype != torch.bfloat16 or kv.dtype != q.dtype:
+        raise RuntimeError(f"q and kv must be bfloat16, got {q.dtype} / {kv.dtype}")
+    if topk_indices.dtype not in (torch.int32, torch.int64):
+        raise RuntimeError(f"topk_indices must be int32 or int64, got {topk_indices.dtype}")
+    for n, x in (("q", q), ("kv", kv), ("topk_indices", topk_indices), ("out", out), ("lse", lse)):
+        if x.is_cuda:
+            raise RuntimeError(f"{n} must be a host (CPU) tensor for the host-buffer call")
+        if not x.is_contiguous():
+            raise RuntimeError(f"{n} must be contiguous")
+    if attn_sink is not None and (attn_sink.is_cuda or attn_sink.dtype != torch.float32):
+        raise RuntimeError("attn_sink must be a float32 host tensor")
+    T, H, _ = q.shape
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise RuntimeError("out must match q's shape and dtype")
+    if tuple(lse.shape) != (T, H) or lse.dtype != torch.float32:
+        raise RuntimeError(f"lse must be float32 [{T}, {H}]")
+    if workspace is None or not workspace.is_cuda:
+        raise RuntimeError("workspace must be a CUDA tensor")
+    if scale is None:
+        scale = 512 ** -0.5
+    idt = SMLA_IDX_INT64 if topk_indices.dtype == torch.int64 else SMLA_IDX_INT32
+    with torch.cuda.device(workspace.device):
+        st = lib().sparse_mla_fwd_host(
+            q.data_ptr(), kv.data_ptr() if kv.numel() else None,
+            topk_indices.data_ptr() if topk_indices.numel() else None, idt,
+            attn_sink.data_ptr() if attn_sink is not None else None, float(scale),
+            out.data_ptr(), lse.data_ptr(), T, H, kv.shape[0], topk_indices.shape[1],
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_ptr(stream))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_fwd_host")
     return out, lse

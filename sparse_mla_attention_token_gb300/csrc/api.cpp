@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "smla_internal.h"
 #include "sparse_mla.h"
@@ -167,9 +168,165 @@ smla_status_t run(const void* q, const void* kv, const void* idx, int32_t index_
   return SMLA_OK;
 }
 
+// Device workspace of the host-buffer call: kv | q | idx | sink | out | lse,
+// each region 256-byte aligned.
+struct HostWs {
+  uint64_t kv, q, idx, sink, out, lse, total;
+};
+
+HostWs host_ws_layout(int64_t T, int32_t H, int32_t topk, int64_t num_kv, int32_t index_dtype,
+                      bool has_sink) {
+  auto up = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
+  const uint64_t isz = index_dtype == SMLA_IDX_INT64 ? 8 : 4;
+  HostWs w{};
+  uint64_t o = 0;
+  w.kv = o;
+  o += up(uint64_t(num_kv) * smla::kHeadDim * 2);
+  w.q = o;
+  o += up(uint64_t(T) * H * smla::kHeadDim * 2);
+  w.idx = o;
+  o += up(uint64_t(T) * topk * isz);
+  w.sink = o;
+  o += up(has_sink ? uint64_t(H) * 4 : 0);
+  w.out = o;
+  o += up(uint64_t(T) * H * smla::kHeadDim * 2);
+  w.lse = o;
+  o += up(uint64_t(T) * H * 4);
+  w.total = o;
+  return w;
+}
+
+// Copy streams and events of the host-buffer call, per device, made on first
+// use and reused (calls enqueue under the lock, so they serialise on them).
+constexpr int kMaxHostChunks = 16;
+struct HostStreams {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in_ev[kMaxHostChunks] = {}, k_ev[kMaxHostChunks] = {};
+};
+
+cudaError_t host_streams(HostStreams** out, std::unique_lock<std::mutex>* lock) {
+  static HostStreams per_dev[64];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  *lock = std::unique_lock<std::mutex>(mu);
+  HostStreams& h = per_dev[dev];
+  if (!h.ready) {
+    if ((e = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    const unsigned f = cudaEventDisableTiming;
+    if ((e = cudaEventCreateWithFlags(&h.start, f)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&h.done, f)) != cudaSuccess) return e;
+    for (int i = 0; i < kMaxHostChunks; ++i) {
+      if ((e = cudaEventCreateWithFlags(&h.in_ev[i], f)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&h.k_ev[i], f)) != cudaSuccess) return e;
+    }
+    h.ready = true;
+  }
+  *out = &h;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
+
+smla_status_t sparse_mla_fwd_host_workspace(int64_t T, int32_t H, int32_t topk, int64_t num_kv,
+                                            int32_t index_dtype, int32_t has_sink,
+                                            uint64_t* bytes) {
+  if (T < 0 || topk < 0 || num_kv < 0 || num_kv >= (int64_t(1) << 31)) return SMLA_ERR_BAD_SHAPE;
+  if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
+  if (index_dtype != SMLA_IDX_INT32 && index_dtype != SMLA_IDX_INT64)
+    return SMLA_ERR_BAD_INDEX_DTYPE;
+  if (bytes == nullptr) return SMLA_ERR_NULL_PTR;
+  *bytes = host_ws_layout(T, H, topk, num_kv, index_dtype, has_sink != 0).total;
+  return SMLA_OK;
+}
+
+smla_status_t sparse_mla_fwd_host(const void* q_host, const void* kv_host,
+                                  const void* topk_indices_host, int32_t index_dtype,
+                                  const float* attn_sink_host, float scale, void* out_host,
+                                  float* lse_host, int64_t T, int32_t H, int64_t num_kv,
+                                  int32_t topk, void* workspace, uint64_t workspace_bytes,
+                                  void* stream) {
+  smla_status_t st = validate(q_host, kv_host, topk_indices_host, index_dtype, attn_sink_host,
+                              scale, out_host, lse_host, T, H, num_kv, topk, nullptr);
+  if (st != SMLA_OK) return st;
+  Plan pl;
+  st = make_plan(T, H, topk, num_kv, 0, &pl);
+  if (st != SMLA_OK) return st;
+  if (T == 0) return SMLA_OK;
+  const HostWs w = host_ws_layout(T, H, topk, num_kv, index_dtype, attn_sink_host != nullptr);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < w.total)
+    return SMLA_ERR_WORKSPACE;
+
+  char* ws = static_cast<char*>(workspace);
+  const uint64_t isz = index_dtype == SMLA_IDX_INT64 ? 8 : 4;
+  const uint64_t q_tok = uint64_t(H) * smla::kHeadDim * 2, i_tok = uint64_t(topk) * isz,
+                 l_tok = uint64_t(H) * 4;
+  // chunks of at least 256 tokens (a full-GPU grid each), at most kMaxHostChunks
+  const int64_t nch = std::max<int64_t>(1, std::min<int64_t>(kMaxHostChunks, T / 256));
+  const int64_t per = (T + nch - 1) / nch;
+
+  HostStreams* hs = nullptr;
+  std::unique_lock<std::mutex> lock;
+  cudaError_t e = host_streams(&hs, &lock);
+  if (e != cudaSuccess) return cuda_fail(e, "host-call streams");
+  cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  // the copies start after the caller's earlier work on `stream`
+  if ((e = cudaEventRecord(hs->start, s0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs->in, hs->start, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs->out, hs->start, 0)) != cudaSuccess)
+    return cuda_fail(e, "host-call ordering");
+  if (num_kv > 0 &&
+      (e = cudaMemcpyAsync(ws + w.kv, kv_host, uint64_t(num_kv) * smla::kHeadDim * 2, h2d,
+                           hs->in)) != cudaSuccess)
+    return cuda_fail(e, "copy in kv");
+  if (attn_sink_host != nullptr &&
+      (e = cudaMemcpyAsync(ws + w.sink, attn_sink_host, uint64_t(H) * 4, h2d, hs->in)) !=
+          cudaSuccess)
+    return cuda_fail(e, "copy in sink");
+  for (int64_t c = 0; c < nch; ++c) {
+    const int64_t t0 = c * per, tc = std::min<int64_t>(per, T - t0);
+    if (tc <= 0) break;
+    if ((e = cudaMemcpyAsync(ws + w.q + t0 * q_tok, static_cast<const char*>(q_host) + t0 * q_tok,
+                             tc * q_tok, h2d, hs->in)) != cudaSuccess ||
+        (topk > 0 && (e = cudaMemcpyAsync(ws + w.idx + t0 * i_tok,
+                                          static_cast<const char*>(topk_indices_host) + t0 * i_tok,
+                                          tc * i_tok, h2d, hs->in)) != cudaSuccess) ||
+        (e = cudaEventRecord(hs->in_ev[c], hs->in)) != cudaSuccess)
+      return cuda_fail(e, "copy in chunk");
+  }
+  for (int64_t c = 0; c < nch; ++c) {
+    const int64_t t0 = c * per, tc = std::min<int64_t>(per, T - t0);
+    if (tc <= 0) break;
+    if ((e = cudaStreamWaitEvent(s0, hs->in_ev[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "chunk ordering");
+    st = run(ws + w.q + t0 * q_tok, num_kv > 0 ? ws + w.kv : nullptr,
+             topk > 0 ? ws + w.idx + t0 * i_tok : nullptr, index_dtype,
+             attn_sink_host != nullptr ? reinterpret_cast<const float*>(ws + w.sink) : nullptr,
+             scale, ws + w.out + t0 * q_tok, reinterpret_cast<float*>(ws + w.lse + t0 * l_tok), tc,
+             H, num_kv, topk, stream, pl.splits, nullptr);   // the whole call's plan
+    if (st != SMLA_OK) return st;
+    if ((e = cudaEventRecord(hs->k_ev[c], s0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hs->out, hs->k_ev[c], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(static_cast<char*>(out_host) + t0 * q_tok, ws + w.out + t0 * q_tok,
+                             tc * q_tok, d2h, hs->out)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(reinterpret_cast<char*>(lse_host) + t0 * l_tok,
+                             ws + w.lse + t0 * l_tok, tc * l_tok, d2h, hs->out)) != cudaSuccess)
+      return cuda_fail(e, "copy out chunk");
+  }
+  // the caller's stream passes this call once the last result is in host memory
+  if ((e = cudaEventRecord(hs->done, hs->out)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(s0, hs->done, 0)) != cudaSuccess)
+    return cuda_fail(e, "host-call completion");
+  return SMLA_OK;
+}
 
 smla_status_t sparse_mla_fwd(const void* q, const void* kv, const void* topk_indices,
                              int32_t index_dtype, const float* attn_sink, float scale,
@@ -298,6 +455,9 @@ const char* sparse_mla_strerror(int32_t status) {
     case SMLA_ERR_SCRATCH_LIMIT:
       return "splits*T*H exceeds the 8192 partial rows of the static scratch "
              "(use sparse_mla_fwd for calls this large)";
+    case SMLA_ERR_WORKSPACE:
+      return "workspace is NULL, smaller than sparse_mla_fwd_host_workspace() or not "
+             "256-byte aligned";
     default: return "unknown status";
   }
 }

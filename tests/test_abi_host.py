@@ -111,3 +111,26 @@ def test_static_scratch_entry_validates_before_cuda(L):
     assert f(*args, 4, 12, 80, 64, None, 2) == 3
     assert f(None, KV, IDX, 0, SINK, 0.04, OUT, LSE, 4, 16, 80, 64, None, 2) == 1
     assert f(*args, 0, 16, 80, 64, None, 2) == 0           # T == 0: nothing to do
+
+
+def test_host_call_workspace_and_validation_before_cuda(L):
+    # workspace bytes: kv | q | idx | sink | out | lse, each rounded up to 256 bytes
+    up = lambda x: (x + 255) // 256 * 256
+    T, H, topk, nkv = 300, 16, 80, 64
+    want = up(nkv * 1024) + up(T * H * 1024) + up(T * topk * 4) + up(H * 4) + up(T * H * 1024) + \
+        up(T * H * 4)
+    assert binding.sparse_mla_fwd_host_workspace(T, H, topk, nkv) == want
+    assert binding.sparse_mla_fwd_host_workspace(T, H, topk, nkv, binding.SMLA_IDX_INT64, False) == \
+        want - up(T * topk * 4) + up(T * topk * 8) - up(H * 4)
+    with pytest.raises(binding.SparseMLAError) as ei:
+        binding.sparse_mla_fwd_host_workspace(T, 12, topk, nkv)
+    assert ei.value.status == 3
+    f = L.sparse_mla_fwd_host
+    args = [Q, KV, IDX, 0, SINK, 0.04, OUT, LSE, T, H, nkv, topk]
+    WS = 0x7f0000400000
+    assert f(*args, None, want, None) == 12                 # no workspace
+    assert f(*args, WS, want - 1, None) == 12               # one byte short
+    assert f(*args, WS + 16, want, None) == 12              # not 256-byte aligned
+    assert f(Q, KV, IDX, 0, SINK, float("nan"), OUT, LSE, T, H, nkv, topk, WS, want, None) == 6
+    assert f(Q, KV, IDX, 0, SINK, 0.04, Q, LSE, T, H, nkv, topk, WS, want, None) == 7
+    assert f(*args[:8], 0, H, nkv, topk, None, 0, None) == 0   # T == 0: nothing to do
