@@ -36,16 +36,18 @@ def _host(x):
     return q, kv, idx, sink
 
 
-@pytest.mark.parametrize("name,T,seed", [("h128", 600, 81), ("h128", 100, 82),
-                                         ("small_head", 1100, 83), ("tiny", 64, 84)])
-def test_host_call_bit_identical(B, name, T, seed):
-    cfg = synth.CONFIGS[name].with_(T=T, seed=seed)
+@pytest.mark.parametrize("name,T,seed,i64", [("h128", 600, 81, False), ("h128", 100, 82, False),
+                                             ("h128", 300, 85, True), ("small_head", 1100, 83, False),
+                                             ("tiny", 64, 84, True)])
+def test_host_call_bit_identical(B, name, T, seed, i64):
+    cfg = synth.CONFIGS[name].with_(T=T, seed=seed, index_dtype="int64" if i64 else "int32")
     x = synth.make_inputs(cfg)
     q, kv, idx, sink = _host(x)
     out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
     lse = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.float32).pin_memory()
     nb = B.sparse_mla_fwd_host_workspace(cfg.T, cfg.H, cfg.topk, cfg.num_kv,
-                                         B.SMLA_IDX_INT32, sink is not None)
+                                         B.SMLA_IDX_INT64 if i64 else B.SMLA_IDX_INT32,
+                                         sink is not None)
     ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
     B.sparse_mla_fwd_host(q, kv, idx, out, lse, sink, ws, x["scale"])
     torch.cuda.current_stream().synchronize()

@@ -182,6 +182,25 @@ def test_head_counts(B, H):
     compare(out, lse, O, L)
 
 
+@pytest.mark.parametrize("idx64", [False, True])
+@pytest.mark.parametrize("H", [16, 64])
+def test_tokens_pipelined_per_cta(B, H, idx64):
+    # More tokens than resident CTAs, so each small-head CTA walks several tokens
+    # and compacts / gathers the next one while computing the current one; lists
+    # of three 32-slot tiles and fully invalid tokens in between (a token
+    # without tiles between tokens with tiles).
+    cfg = synth.CONFIGS["tiny"].with_(T=700, H=H, pool=300, ratio=1, topk=96, window=40,
+                                      index_dtype="int64" if idx64 else "int32", seed=17)
+    x = synth.make_inputs(cfg)
+    idx = x["idx"].copy()
+    idx[3::7] = -1
+    idx[5::11, ::2] = cfg.num_kv + 7
+    x["idx"] = idx
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
 @pytest.mark.parametrize("H", HEADS)
 @pytest.mark.parametrize("topk,window", [(1, 1), (3, 2), (67, 40), (130, 64), (2048, 150),
                                          (2500, 200)])
