@@ -61,21 +61,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// Packed fp16x2 -> the two floats (exact).
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&v));
-}
-// The same widening on the integer and FMA pipes (no conversion unit), for
-// finite fp16 values: the 15 exponent+mantissa bits move to the top of an
-// fp32 mantissa-aligned field (an fp32 whose exponent is 112 too small; fp16
-// subnormals land on fp32 subnormals) and one exact multiply by 2^112
-// restores the exponent.  Needs the default no-flush-to-zero multiply.
-__device__ __forceinline__ float2 unpack_f16x2_alu(uint32_t v) {
-  const uint32_t lo = ((v & 0x7FFFu) << 13) | ((v & 0x8000u) << 16);
-  const uint32_t hi = ((v >> 3) & 0x0FFFE000u) | (v & 0x80000000u);
-  return make_float2(__uint_as_float(lo) * 0x1p112f, __uint_as_float(hi) * 0x1p112f);
-}
-
 // f16(a) + f16(b) in fp32 for both halves of two packed fp16x2 words: each
 // half of b is widened exactly (b + 0), then added to the matching half of a
 // with one fp32 rounding (mixed-precision add, sm_100 family).

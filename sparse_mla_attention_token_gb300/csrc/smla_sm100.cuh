@@ -1,6 +1,7 @@
 // Blackwell (sm_100 family, built for sm_103a) PTX wrappers: mbarriers with
-// bounded waits, TMA tile and gather4 loads, tcgen05 (TMEM alloc, MMA,
-// commit, ld/st, fences), cluster shared-memory access.
+// bounded waits, TMA tile loads / stores and L2 prefetch, bulk-group waits,
+// tcgen05 (TMEM alloc, MMA, commit, ld/st, fences), cluster shared-memory
+// access (mapa, st.async, remote arrives).
 #pragma once
 
 #include <cuda.h>
@@ -23,11 +24,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// arrive on a barrier of another CTA of the cluster (address from mapa), release at cluster scope
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
 }
 // non-blocking: has the phase with this parity completed?
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
@@ -95,11 +91,6 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
 
 // 16-byte asynchronous store into another CTA of the cluster; its byte count
 // is credited (complete_tx) to `cluster_bar`, a barrier of that same CTA.
@@ -109,15 +100,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint4 v, uint
           cluster_addr),
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
       : "memory");
-}
-// Per-warpgroup register budget changes (all 128 threads of the warpgroup).
-template <uint32_t kRegs>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-template <uint32_t kRegs>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 // Named barrier among `nthreads` threads (whole warps) of the CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
@@ -131,16 +113,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-// four rows (r0..r3) of one column box, landing as 4 consecutive box rows at dst
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(bar)
       : "memory");
 }
 // 2-D tile store shared::cta -> global, tracked by this thread's bulk groups
