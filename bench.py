@@ -278,6 +278,15 @@ def run_ours(args, cfg) -> None:
         raise RuntimeError("device status not OK after the timed steps")
     total_ms = sum(step_ms)
     max_total_ms = sdist.max_over_ranks(total_ms, dev)
+    # warm-L2 reference (not the headline): the same call back to back without the flush
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(min(K, 20))]
+    for a, b in wev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = [a.elapsed_time(b) for a, b in wev]
     all_flops = sdist.sum_over_ranks(counts.flops, dev)
     value = all_flops * K / (max_total_ms * 1e-3) / 1e12
 
@@ -350,7 +359,8 @@ def run_ours(args, cfg) -> None:
             "e2e": e2e, "gpu_launches": K * launches, "clocks": clocks, "roofline": roof,
             "roofline_terms": t,
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
-                        "max": max(step_ms)}}
+                        "max": max(step_ms),
+                        "warm_l2_median": statistics.median(warm_ms) if warm_ms else None}}
     if world == 1 and rank == 0 and args.cpu_seconds > 0:
         r = oracle_rate(x, cfg, args.cpu_seconds)
         line["cpu_baseline"] = {
