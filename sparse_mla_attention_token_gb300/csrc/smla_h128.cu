@@ -9,9 +9,13 @@
 // one 256-wide half of the head dim (rank r: columns 256r..256r+255):
 //   * S_r = Q[:, half r] . K[:, half r]^T, its partial scores over that half;
 //   * the pair swaps partials: each CTA scales its partial to base-2 logits,
-//     rounds it to fp16, sends it with st.async (the bytes are counted on the
-//     peer's mbarrier, so no fence per thread is needed) and forms
-//     S = f16(S_0) + f16(S_1) in fp32, which is bit-identical in both CTAs;
+//     takes each row's maximum o_r off it, rounds the remainder to fp16 and
+//     sends remainder and o_r with st.async (the bytes are counted on the
+//     peer's mbarrier, so no fence per thread is needed); both form
+//     S = f16(S_0 - o_0) + f16(S_1 - o_1) relative to o_0 + o_1 in fp32,
+//     bit-identical in both CTAs.  Taking the row maximum off first makes the
+//     rounding error depend on how far a score lies below its row's top (as
+//     softmax does), not on the size of the logits;
 //   * both CTAs run the same online softmax on the same S;
 //   * O[:, half r] += P . V[:, half r] into its own TMEM.
 //   TMEM per CTA: O half 256 columns, three 64-column S buffers, two
@@ -85,8 +89,12 @@ constexpr uint32_t kStgBytes = 32 * 32 * 2;                  // 2 KB per block
 constexpr uint32_t kRowsOff = kStgOff + 8 * kStgBytes;       // int32 row lists
 constexpr uint32_t kMaxOff = kRowsOff + 2 * kMaxTopk * 4;    // running max handoff [2][128]
 constexpr uint32_t kSumOff = kMaxOff + 2 * 128 * 4;          // epilogue sums [2][2][2][128]
-constexpr uint32_t kBarOff = kSumOff + 2 * 512 * 4;
+constexpr uint32_t kXMaxOff = kSumOff + 2 * 512 * 4;         // peer row maxima: [2][128] fp32
+constexpr uint32_t kXMaxBytes = 128 * 4;
+constexpr uint32_t kXTxBytes = kXBufBytes + kXMaxBytes;      // bytes a peer sends per tile
+constexpr uint32_t kBarOff = kXMaxOff + kXBufs * kXMaxBytes;
 constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 constexpr long long kTimeoutCycles = 4000000000LL;    // ~2 s at 2 GHz
 
@@ -586,15 +594,42 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
 }
 
+// Largest / smallest of a row's 64 raw fp32 partial scores (bit patterns).
+__device__ __forceinline__ float row_max64(const uint32_t* v) {
+  float t[22];
+#pragma unroll
+  for (int k = 0; k < 21; ++k)
+    t[k] = max3f(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]), __uint_as_float(v[3 * k + 2]));
+  t[21] = __uint_as_float(v[63]);
+  float u[8];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) u[k] = max3f(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
+  u[7] = t[21];
+  return max3f(max3f(u[0], u[1], u[2]), max3f(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+}
+__device__ __forceinline__ float row_min64(const uint32_t* v) {
+  float t[22];
+#pragma unroll
+  for (int k = 0; k < 21; ++k)
+    t[k] = min3f(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]), __uint_as_float(v[3 * k + 2]));
+  t[21] = __uint_as_float(v[63]);
+  float u[8];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) u[k] = min3f(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
+  u[7] = t[21];
+  return min3f(min3f(u[0], u[1], u[2]), min3f(u[3], u[4], u[5]), fminf(u[6], u[7]));
+}
+
 // Warps 8-15: two score warpgroups.  Warpgroup w handles the tiles g with
 // g % 2 == w (tile numbers count every tile of this CTA); thread = TMEM lane =
 // head `row`.  For its tile g a warpgroup
-//   1. reads this CTA's partial scores S_r(g) (64 fp32) from S buffer g%3,
-//      rounds them to fp16 and frees the buffer;
-//   2. st.asyncs them into the peer's receive buffer g%3 (the bytes are
-//      counted on the peer's mbarrier);
-//   3. once the peer's partials are in, forms S = f16(S_0) + f16(S_1) in fp32
-//      (the same value in both CTAs);
+//   1. reads this CTA's partial scores S_r(g) (64 fp32) from S buffer g%3 and
+//      frees the buffer; scales them to base-2 logits, takes the row's largest
+//      o_r off and rounds the remainder to fp16;
+//   2. st.asyncs remainder and o_r into the peer's receive buffer g%2 (the
+//      bytes are counted on the peer's mbarrier);
+//   3. once the peer's are in, forms S - off = f16(S_0 - o_0) + f16(S_1 - o_1)
+//      in fp32 with off = o_0 + o_1 (the same values in both CTAs);
 //   4. takes the running max: it waits for the max the other warpgroup
 //      settled for tile g-1 (per row, through shared memory), raises it only
 //      when the tile's max exceeds it by more than 2^8, and publishes it for
@@ -616,11 +651,14 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
   const float sl2 = p.scale * kLog2e;
   float* m_sh = reinterpret_cast<float*>(base + kMaxOff);   // [2 tile parities][128]
   float* l_sh = reinterpret_cast<float*>(base + kSumOff);   // [2 tokens][2 wg][2 (l, m)][128]
+  const float* xmax_sh = reinterpret_cast<const float*>(base + kXMaxOff);   // [2][128]
   uint32_t recv_local[kXBufs], recv_peer[kXBufs], xfull_peer[kXBufs], xfree_peer[kXBufs];
+  uint32_t xmax_peer[kXBufs];
 #pragma unroll
   for (int i = 0; i < kXBufs; ++i) {
     recv_local[i] = sbase + kXOff + i * kXBufBytes + row * 128;
     recv_peer[i] = map_peer(recv_local[i], peer);
+    xmax_peer[i] = map_peer(sbase + kXMaxOff + (i * 128 + row) * 4, peer);
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
     xfree_peer[i] = map_peer(bar_addr(b->x_free[i]), peer);
   }
@@ -648,7 +686,9 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
         break;
       if (row == 0) SMLA_TL(2, g, 0);
       tc_fence_after();
+      const int nvt = min(kTileN, nv - j * kTileN);   // valid columns of this tile
       uint32_t own[32];
+      float o_own;   // this row's largest scaled partial: o_own - (what was sent) is the partial
       {
         uint32_t sv[64];
         tmem_ld32(tl + kTmemS + sb * kTileN, sv);
@@ -656,11 +696,20 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar_addr(b->s_free[sb]));
-        // scaled to base-2 logits before the rounding (keeps fp16's range for large scores)
+        // the row's top partial in base-2 logits over the valid columns (rounding
+        // is monotone, so the extreme raw value scales to the largest scaled one;
+        // a negative scale turns the smallest raw value into it).  The zero-filled
+        // tail of a ragged tile takes column 0's value, which changes neither.
+        if (nvt < kTileN) {
+#pragma unroll
+          for (int i = 1; i < 64; ++i) sv[i] = (i < nvt) ? sv[i] : sv[0];
+        }
+        o_own = sl2 * (sl2 >= 0.f ? row_max64(sv) : row_min64(sv));
+        // S sl2 - o_own in one rounding, then fp16
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float2 t = mul2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
-                                make_float2(sl2, sl2));
+          const float2 t = fma2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                make_float2(sl2, sl2), make_float2(-o_own, -o_own));
           own[i] = pack_f16x2(t.x, t.y);
         }
       }
@@ -675,14 +724,16 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
         st_async_v4(recv_peer[xb] + ((c ^ (row & 7)) << 4),
                     make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
                     xfull_peer[xb]);
-      if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXBufBytes);
+      st_async_b32(xmax_peer[xb], __float_as_uint(o_own), xfull_peer[xb]);
+      if (row == 0) mbar_arrive_expect_tx(bar_addr(b->x_full[xb]), kXTxBytes);
       if (row == 0) SMLA_TL(2, g, 1);
       // 3. the peer's partial scores; full base-2 scores, tail masked
       if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar_addr(b->x_full[xb]),
                                                         (g / kXBufs) & 1, b, p.err, 8u))))
         break;
       if (row == 0) SMLA_TL(2, g, 2);
-      const int nvt = min(kTileN, nv - j * kTileN);
+      // scores relative to off = o_0 + o_1 (the same sum in both CTAs)
+      const float off = o_own + xmax_sh[xb * 128 + row];
       float s[64];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -713,7 +764,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
 #pragma unroll
         for (int k = 0; k < 7; ++k) u[k] = max3f(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
         u[7] = t[21];
-        mx = max3f(max3f(u[0], u[1], u[2]), max3f(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+        mx = max3f(max3f(u[0], u[1], u[2]), max3f(u[3], u[4], u[5]), fmaxf(u[6], u[7])) + off;
       }
       float m_prev = -INFINITY;
       if (g >= 1) {
@@ -729,13 +780,14 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
       m_sh[(g & 1) * 128 + row] = m_new;
       mbar_arrive(bar_addr(b->m_ready[g & 1][qd]));
       if (row == 0) SMLA_TL(2, g, 3);
-      // 5. P = 2^(S - m), this warpgroup's sum
+      // 5. P = 2^(S - m), this warpgroup's sum (s holds S - off)
+      const float m_rel = m_new - off;
       float2 sum4[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) sum4[k] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float2 t = add2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(-m_new, -m_new));
+        float2 t = add2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(-m_rel, -m_rel));
         t.x = ex2(t.x);
         t.y = ex2(t.y);
         s[2 * i] = t.x;

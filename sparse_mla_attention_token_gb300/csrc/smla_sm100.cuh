@@ -101,6 +101,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint4 v, uint
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
       : "memory");
 }
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
+      "r"(v), "r"(cluster_bar)
+      : "memory");
+}
 // Named barrier among `nthreads` threads (whole warps) of the CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -45,8 +45,11 @@ def to_dev(x, dev, kv_offset_bytes: int = 0, guard_rows: int = 0, guard_value=No
     return q, kv, idx, sink, keep
 
 
-def compare(out, lse, O, L, tokens=None):
-    """Return a dict of parity numbers; raises AssertionError outside the bar."""
+def compare(out, lse, O, L, tokens=None, o_tol=TOL_O):
+    """Return a dict of parity numbers; raises AssertionError outside the bar.
+
+    ``o_tol`` replaces the max|dO| bar for callers that check O themselves.
+    """
     og = out.float().cpu().numpy().astype(np.float64)
     lg = lse.float().cpu().numpy().astype(np.float64)
     if tokens is not None:
@@ -65,7 +68,7 @@ def compare(out, lse, O, L, tokens=None):
     nab = np.sqrt((a * a).sum() * (b * b).sum())
     cos = float((a * b).sum() / nab) if nab > 0 else 1.0
     res = {"max_dO": d_o, "max_dlse": d_l, "cos": cos}
-    assert d_o <= TOL_O, f"max|dO| {d_o} > {TOL_O} ({res})"
+    assert d_o <= o_tol, f"max|dO| {d_o} > {o_tol} ({res})"
     assert d_l <= TOL_LSE, f"max|dlse| {d_l} > {TOL_LSE} ({res})"
     assert cos >= TOL_COS, f"cos {cos} < {TOL_COS} ({res})"
     return res

@@ -294,6 +294,38 @@ def test_h128_token_counts(B, T):
     compare(out, lse, O, L)
 
 
+def _bf16_of(f):
+    return synth.bf16_bits(np.asarray(f, np.float32))
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+@pytest.mark.parametrize("case", ["q_times_4", "common_shift_25"])
+def test_h128_large_logits(B, case, splits):
+    # Logits well above the N(0,1) recipe's: q scaled by 4 (natural scores of
+    # standard deviation 4), or a score component of about 25 shared by every
+    # kv row of a token (a direction common to q and kv).  The tcgen05 kernel
+    # rounds each half's partial scores to fp16 after taking the row's largest
+    # off, so a shared component costs it no precision.
+    cfg = synth.CONFIGS["h128"].with_(T=200, seed=43)
+    x = synth.make_inputs(cfg)
+    q = orc.bf16_to_f64(x["q"])
+    if case == "q_times_4":
+        x["q"] = _bf16_of(4.0 * q)          # exact: a power of two
+    else:
+        u = np.zeros(512)
+        u[0::2] = 1.0 / np.sqrt(256.0)
+        x["kv"] = _bf16_of(orc.bf16_to_f64(x["kv"]) + 4.0 * u)
+        x["q"] = _bf16_of(q + (25.0 / 4.0) * np.sqrt(512.0) * u)
+    out, lse, _ = _run(B, x, splits=splits)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    # Peaked softmax puts |O| up to about 5, where half a bf16 step of the
+    # output alone is 2^-6: O is held to the bar plus one bf16 step of |O|
+    # (output rounding and P's bf16 rounding); lse and the cosine to the bar.
+    og = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(og - O) <= 2e-2 + 2.0 ** -8 * np.abs(O))
+    compare(out, lse, O, L, o_tol=np.inf)
+
+
 def test_h128_vs_split_path(B):
     cfg = synth.CONFIGS["h128"].with_(T=300, seed=41)
     x = synth.make_inputs(cfg)
