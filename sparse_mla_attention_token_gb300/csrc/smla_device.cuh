@@ -61,33 +61,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// f16(a) + f16(b) in fp32 for both halves of two packed fp16x2 words: each
-// half of b is widened exactly (b + 0), then added to the matching half of a
-// with one fp32 rounding (mixed-precision add, sm_100 family).
-__device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
-  float2 r;
-  asm("{\n.reg .f16 a0, a1, b0, b1;\n.reg .f32 t0, t1;\n"
-      "mov.b32 {a0, a1}, %2;\n"
-      "mov.b32 {b0, b1}, %3;\n"
-      "add.rn.f32.f16 t0, b0, 0f00000000;\n"
-      "add.rn.f32.f16 t1, b1, 0f00000000;\n"
-      "add.rn.f32.f16 %0, a0, t0;\n"
-      "add.rn.f32.f16 %1, a1, t1;\n}"
-      : "=f"(r.x), "=f"(r.y)
-      : "r"(a), "r"(b));
-  return r;
-}
 // Packed fp32 pair arithmetic (one instruction for two lanes of work, sm_100 family).
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n.reg .b64 x, y, z;\n"
-      "mov.b64 x, {%2, %3};\nmov.b64 y, {%4, %5};\n"
-      "mul.rn.f32x2 z, x, y;\n"
-      "mov.b64 {%0, %1}, z;\n}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   float2 r;
   asm("{\n.reg .b64 x, y, z;\n"
@@ -96,6 +70,18 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
       "mov.b64 {%0, %1}, z;\n}"
       : "=f"(r.x), "=f"(r.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+// a + f16(b) in fp32 for both halves of a packed fp16x2 word (mixed-precision
+// add, one rounding each)
+__device__ __forceinline__ float2 add_f32_f16x2(float2 a, uint32_t b) {
+  float2 r;
+  asm("{\n.reg .f16 b0, b1;\n"
+      "mov.b32 {b0, b1}, %4;\n"
+      "add.rn.f32.f16 %0, b0, %2;\n"
+      "add.rn.f32.f16 %1, b1, %3;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "r"(b));
   return r;
 }
 // a * b + c on both halves, one rounding each (packed fma, sm_100 family)

@@ -11,12 +11,14 @@
 //   * the pair swaps partials: each CTA scales its partial to base-2 logits,
 //     takes each row's maximum o_r off it, rounds the remainder to fp16 and
 //     sends remainder and o_r with st.async (the bytes are counted on the
-//     peer's mbarrier, so no fence per thread is needed); both form
-//     S = f16(S_0 - o_0) + f16(S_1 - o_1) relative to o_0 + o_1 in fp32,
-//     bit-identical in both CTAs.  Taking the row maximum off first makes the
+//     peer's mbarrier, so no fence per thread is needed); CTA r forms
+//     S = (S_r - o_r) + f16(S_peer - o_peer) relative to o_0 + o_1 in fp32,
+//     its own remainder unrounded.  Taking the row maximum off first makes the
 //     rounding error depend on how far a score lies below its row's top (as
 //     softmax does), not on the size of the logits;
-//   * both CTAs run the same online softmax on the same S;
+//   * each CTA runs the online softmax on its S (the two differ only by the
+//     rounding of one half's remainder; P, l and the O half of a CTA all come
+//     from the same S, and rank 0 writes lse);
 //   * O[:, half r] += P . V[:, half r] into its own TMEM.
 //   TMEM per CTA: O half 256 columns, three 64-column S buffers, two
 //   32-column P buffers (bf16 pairs, the A operand of P.V).
@@ -628,8 +630,8 @@ __device__ __forceinline__ float row_min64(const uint32_t* v) {
 //      o_r off and rounds the remainder to fp16;
 //   2. st.asyncs remainder and o_r into the peer's receive buffer g%2 (the
 //      bytes are counted on the peer's mbarrier);
-//   3. once the peer's are in, forms S - off = f16(S_0 - o_0) + f16(S_1 - o_1)
-//      in fp32 with off = o_0 + o_1 (the same values in both CTAs);
+//   3. once the peer's are in, forms S - off = (S_r - o_r) + f16(S_peer - o_peer)
+//      in fp32 with off = o_0 + o_1 (its own remainder unrounded);
 //   4. takes the running max: it waits for the max the other warpgroup
 //      settled for tile g-1 (per row, through shared memory), raises it only
 //      when the tile's max exceeds it by more than 2^8, and publishes it for
@@ -687,6 +689,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
       if (row == 0) SMLA_TL(2, g, 0);
       tc_fence_after();
       const int nvt = min(kTileN, nv - j * kTileN);   // valid columns of this tile
+      float2 ownf[32];   // this CTA's remainders, kept in fp32
       uint32_t own[32];
       float o_own;   // this row's largest scaled partial: o_own - (what was sent) is the partial
       {
@@ -710,6 +713,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
         for (int i = 0; i < 32; ++i) {
           const float2 t = fma2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
                                 make_float2(sl2, sl2), make_float2(-o_own, -o_own));
+          ownf[i] = t;
           own[i] = pack_f16x2(t.x, t.y);
         }
       }
@@ -732,7 +736,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
                                                         (g / kXBufs) & 1, b, p.err, 8u))))
         break;
       if (row == 0) SMLA_TL(2, g, 2);
-      // scores relative to off = o_0 + o_1 (the same sum in both CTAs)
+      // scores relative to off = o_0 + o_1
       const float off = o_own + xmax_sh[xb * 128 + row];
       float s[64];
 #pragma unroll
@@ -742,7 +746,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
         const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float2 t = add_f16x2_f32(own[4 * c + q], pv[q]);   // f16(own) + f16(peer)
+          const float2 t = add_f32_f16x2(ownf[4 * c + q], pv[q]);   // own + f16(peer)
           s[8 * c + 2 * q] = t.x;
           s[8 * c + 2 * q + 1] = t.y;
         }
