@@ -326,6 +326,22 @@ def test_h128_large_logits(B, case, splits):
     compare(out, lse, O, L, o_tol=np.inf)
 
 
+@pytest.mark.parametrize("scale", [-1.0 / np.sqrt(512.0), -2.0 / np.sqrt(512.0), 0.0])
+@pytest.mark.parametrize("H,splits", [(16, 0), (128, 0), (128, 2)])
+def test_scale_sign_and_zero(B, H, splits, scale):
+    # Scale is an argument and may be negative or zero (PR #6002 dropped the
+    # positivity check).  A negative scale turns each row's smallest raw score
+    # into its largest logit, which the H = 128 kernel's row maximum has to
+    # follow; zero makes every score 0 (weights 1 / (n + e^sink)).  Lists of up
+    # to 150 slots: several 64-slot tiles with a ragged last one.
+    cfg = synth.CONFIGS["tiny"].with_(T=200, H=H, pool=200, ratio=1, topk=150, window=48, seed=23)
+    x = synth.make_inputs(cfg)
+    x["scale"] = float(scale)
+    out, lse, _ = _run(B, x, splits=splits)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
 def test_h128_vs_split_path(B):
     cfg = synth.CONFIGS["h128"].with_(T=300, seed=41)
     x = synth.make_inputs(cfg)
