@@ -20,15 +20,22 @@
 //     rounding of one half's remainder; P, l and the O half of a CTA all come
 //     from the same S, and rank 0 writes lse);
 //   * O[:, half r] += P . V[:, half r] into its own TMEM.
-//   TMEM per CTA: O half 256 columns, three 64-column S buffers, two
-//   32-column P buffers (bf16 pairs, the A operand of P.V).
+//   TMEM per CTA: O half 256 columns, two 64-column S buffers, two 32-column
+//   P buffers (bf16 pairs, the A operand of P.V) and the first 128 of the
+//   half's Q columns (64 columns of bf16 pairs, the A operand of the first 8
+//   of S's 16 MMAs; the other 128 Q columns stay in shared memory).  Holding
+//   part of Q in TMEM frees the shared memory for a fourth KV stage: a stage
+//   is busy from its gather through S, the score exchange and softmax to its
+//   P.V, so the ring's depth sets how many tiles are in flight.
 //
 // Data movement.  Producer warp 0 compacts the token's valid slots
 // (0 <= idx < num_kv at the index's full width; PR #6002 "Invalid KV rows",
-// "int64 indices") into a row list one token ahead and loads the token's Q
-// half with 2-D TMA.  Producer warps 0-6 gather each tile's 64 half rows
+// "int64 indices") into a row list one token ahead and loads Q columns 0-127
+// of the token's half with 2-D TMA into a 32 KB buffer; the MMA thread copies
+// them into TMEM (tcgen05.cp) and then loads columns 128-255 into the same
+// buffer.  Producer warps 0-6 gather each tile's 64 half rows
 // (512 B each) with 16-byte cp.async straight into the 128-byte-swizzled
-// layout of a 3-stage ring; each fences its landed copies into the async
+// layout of a 4-stage ring; each fences its landed copies into the async
 // proxy before it arrives on the stage's barrier.  One tile serves as the
 // K-major B operand of Q.K^T and the MN-major B operand of P.V.  The ragged
 // tail of a token's last tile is zero-filled and its scores are masked: no
@@ -71,16 +78,17 @@ constexpr int kMmaWarp = 7;
 constexpr int kScoreWarp0 = 8;        // warps 8-15: two score warpgroups
 constexpr int kWgThreads = 128;       // one thread per head row
 constexpr int kTileN = 64;            // slots per tile
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 3;
-constexpr uint32_t kTmemS = 256;      // three S buffers (64 columns each)
-constexpr uint32_t kTmemP = 448;      // two P buffers (32 columns of bf16 pairs each); O at 0
+constexpr int kSBufs = 2;
+constexpr uint32_t kTmemS = 256;      // two S buffers (64 columns each); O at 0
+constexpr uint32_t kTmemP = 384;      // two P buffers (32 columns of bf16 pairs each)
+constexpr uint32_t kTmemQ = 448;      // Q columns 0-127 of this CTA's half (64 columns of bf16 pairs)
 
 // shared memory layout (offsets from a 1024-byte aligned base)
-constexpr uint32_t kQOff = 0;                         // [4 col blocks][128 rows][128 B]
-constexpr uint32_t kQBytes = 128 * 256 * 2;           // 64 KB
+constexpr uint32_t kQOff = 0;                         // [2 col blocks][128 rows][128 B]
+constexpr uint32_t kQBytes = 128 * 128 * 2;           // 32 KB: Q columns 0-127 (staged for TMEM), then 128-255
 constexpr uint32_t kKVOff = kQOff + kQBytes;          // [stage][4 col blocks][64 rows][128 B]
 constexpr uint32_t kStageBytes = kTileN * 256 * 2;    // 32 KB
 constexpr uint32_t kXOff = kKVOff + kStages * kStageBytes;   // peer partials: [2][128][64 fp16]
@@ -101,7 +109,9 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr long long kTimeoutCycles = 4000000000LL;    // ~2 s at 2 GHz
 
 struct Bars {
-  uint64_t q_full, q_empty;
+  uint64_t q_lo_full, q_hi_full;   // Q columns 0-127 / 128-255 of the half landed (TMA)
+  uint64_t qcp_done;               // Q columns 0-127 copied into TMEM (MMA commit)
+  uint64_t q_empty;                // the token's last S has completed
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[kSBufs];   // partial S(g) in TMEM (MMA commit)
   uint64_t s_free[kSBufs];   // the score warpgroup has read S(g)
@@ -350,11 +360,13 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
                         wait_bar<false>(bar_addr(b->q_empty), (qn & 1) ^ 1, b, p.err, 1u));
         if (ok && lane == 0) {
           SMLA_TL(0, gt, 3);
-          mbar_arrive_expect_tx(bar_addr(b->q_full), kQBytes);
+          // columns 0-127 of the half; the MMA thread copies them into TMEM and
+          // then loads columns 128-255 into the same buffer
+          mbar_arrive_expect_tx(bar_addr(b->q_lo_full), kQBytes);
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb)
+          for (int cb = 0; cb < 2; ++cb)
             tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 64 * cb,
-                        static_cast<int>(tok * 128), bar_addr(b->q_full));
+                        static_cast<int>(tok * 128), bar_addr(b->q_lo_full));
           ++q_loads;
           // the next token's Q half into L2 now, so its load at the token switch is short
           if (tok + ncl < p.T) {
@@ -464,7 +476,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
   if (epi_warp && lane == 0) bulk_wait<0>();   // every O block stored before the CTA exits
   cp_async_wait<0>();   // drain: no copy of ours may land after the CTA exits
   if (warp == 0 && lane == 0 && q_loads > 0)
-    wait_bar<false, true>(bar_addr(b->q_full), (q_loads - 1) & 1, b, p.err, 1u);
+    wait_bar<false, true>(bar_addr(b->q_lo_full), (q_loads - 1) & 1, b, p.err, 1u);
 }
 
 // Warp 3, lane 0: issues every tcgen05.mma of the CTA.
@@ -475,7 +487,8 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
 // next S has its inputs and issues whichever is ready, P.V first because it
 // releases a KV stage.  No operation waits behind another one's inputs.  A
 // pass without progress for ~2 s (or another role giving up) ends the loop.
-__device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem) {
+__device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t tmem,
+                         const CUtensorMap* tm_q, uint32_t rank) {
   const uint32_t sbase = smem_u32(base);
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTileN, false, false);
@@ -486,7 +499,9 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   int64_t tok = cid;
   int it = 0;                 // token iteration (meta slot / parity)
   int nt = 0, j = 0;          // tiles of the current token, next tile index in it
-  bool have_meta = false, have_q = false;
+  bool have_meta = false;
+  int q_state = 0;            // 0: wait Q low half, 1: copy done?, 2: wait Q high half, 3: Q ready
+  uint32_t hi_loads = 0;      // Q high-half loads issued
   uint32_t qn = 0, tokn = 0;  // tokens with tiles: Q loads consumed, token index
   uint32_t sg = 0;            // next S tile (global)
   // P.V side
@@ -531,7 +546,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
           nt = (nv + kTileN - 1) / kTileN;
           j = 0;
           have_meta = true;
-          have_q = false;
+          q_state = 0;
           progress = true;
           if (nt == 0) {   // nothing to compute for this token
             have_meta = false;
@@ -539,11 +554,36 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
             ++it;
           }
         }
-      } else if (!have_q) {
-        if (mbar_test_wait(bar_addr(b->q_full), qn & 1)) {
+      } else if (q_state == 0) {
+        // Q columns 0-127 landed (loaded once the previous token's last S completed):
+        // into TMEM, 16 K elements (8 columns) per copy
+        if (mbar_test_wait(bar_addr(b->q_lo_full), qn & 1)) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tmem_cp_128x256b(tmem + kTmemQ + 8 * kk,
+                             sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024));
+          mma_commit(bar_addr(b->qcp_done));
+          q_state = 1;
+          progress = true;
+        }
+      } else if (q_state == 1) {
+        // the copies have read the buffer: columns 128-255 into it
+        if (mbar_test_wait(bar_addr(b->qcp_done), qn & 1)) {
+          mbar_arrive_expect_tx(bar_addr(b->q_hi_full), kQBytes);
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 128 + 64 * cb,
+                        static_cast<int>(tok * 128), bar_addr(b->q_hi_full));
+          ++hi_loads;
+          q_state = 2;
+          progress = true;
+        }
+      } else if (q_state == 2) {
+        if (mbar_test_wait(bar_addr(b->q_hi_full), qn & 1)) {
           SMLA_TL(1, sg, 5);
           tc_fence_after();
-          have_q = true;
+          q_state = 3;
           progress = true;
         }
       } else {
@@ -557,9 +597,14 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk) {
             const uint32_t koff = (kk & 3) * 32;   // 16 K elements = 32 B inside a 128 B row
-            const uint64_t a = sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + koff, 16, 1024);
             const uint64_t bd = sdesc_sw128(kv + (kk >> 2) * 8192 + koff, 16, 1024);
-            mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+            if (kk < 8) {   // Q columns 0-127 from TMEM
+              mma_bf16_ts(tmem + kTmemS + sb * kTileN, tmem + kTmemQ + 8 * kk, bd, kIdescS,
+                          kk > 0 ? 1u : 0u);
+            } else {        // Q columns 128-255 from shared memory
+              const uint64_t a = sdesc_sw128(sbase + kQOff + ((kk - 8) >> 2) * 16384 + koff, 16, 1024);
+              mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, 1u);
+            }
           }
           mma_commit(bar_addr(b->s_full[sb]));
           SMLA_TL(1, sg, 0);
@@ -591,9 +636,11 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
       __nanosleep(32);   // leave issue slots to the warps sharing this sub-partition
     }
   }
-  // drain: every MMA issued must complete before TMEM is freed
+  // drain: every MMA and copy issued must complete before TMEM is freed, and
+  // no Q load of ours may land after the CTA exits
   mma_commit(bar_addr(b->drain));
   wait_bar<false, true>(bar_addr(b->drain), 0, b, p.err, 2u);
+  if (hi_loads > 0) wait_bar<false, true>(bar_addr(b->q_hi_full), (hi_loads - 1) & 1, b, p.err, 2u);
 }
 
 // Largest / smallest of a row's 64 raw fp32 partial scores (bit patterns).
@@ -862,7 +909,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_addr(b->q_full), 1);
+    mbar_init(bar_addr(b->q_lo_full), 1);
+    mbar_init(bar_addr(b->q_hi_full), 1);
+    mbar_init(bar_addr(b->qcp_done), 1);
     mbar_init(bar_addr(b->q_empty), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_addr(b->kv_full[s]), kProducerThreads);
@@ -906,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kMmaWarp) {
     producer_role<IdxT>(p, &tm_q, &tm_o, base, b, tmem, rank, warp, lane);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role(p, base, b, tmem);
+    if (lane == 0) mma_role(p, base, b, tmem, &tm_q, rank);
     __syncwarp();
   } else {
     score_role(p, base, b, tmem, rank, warp, lane);
