@@ -323,10 +323,10 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
       uint32_t w16[16];
       load(cc, w16);
       put(cc, w16, cc - kHeld);
-      if (cc == kHeld) mid();
     }
     tc_fence_before();
     mbar_arrive(bar_addr(b->o_free));   // all of O has been read
+    mid();
 #pragma unroll
     for (int cc = 0; cc < kHeld; ++cc) put(cc, held[cc], 8 - kHeld + cc);
     if (lane == 0) SMLA_TL(3, ep_gl, 6);
@@ -398,15 +398,19 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
       for (int j = 0; j < ntiles; ++j) {
         const uint32_t g = gt + j;
         const uint32_t s = g % kStages, ph = (g / kStages) & 1;
-        // this stage is freed by P.V(g - kStages); if that P.V belongs to a
-        // token after the pending one, it waits for O: run the epilogue now
-        if (epi_warp && ep_pend && g >= ep_gl + 1 + kStages) {
-          if (pending >= 0) {
-            cp_async_wait<0>();
-            land_and_arrive(bar_addr(b->kv_full[pending]));
-            pending = -1;
-          }
-          if (!(run = epilogue([]() {}))) break;
+        // this stage is freed by P.V(g - kStages): once that is the pending
+        // token's last P.V (or a later one), run the token's epilogue before
+        // waiting for the stage, and count the previous tile's copies once O
+        // has been released
+        if (epi_warp && ep_pend && g >= ep_gl + kStages) {
+          if (!(run = epilogue([&]() {
+                if (pending >= 0) {
+                  cp_async_wait<0>();
+                  land_and_arrive(bar_addr(b->kv_full[pending]));
+                  pending = -1;
+                }
+              })))
+            break;
         }
         // Overlap the previous tile's copies with this issue only if this
         // stage is already free; otherwise count them first, so a tile's
@@ -444,16 +448,6 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
           if (lane == 0) SMLA_TL(0, g - 1, 2);
         }
         pending = static_cast<int>(s);
-        // this tile's stage was freed by the pending token's last P.V: run its
-        // epilogue now (counting this tile's copies once they have landed, mid-way)
-        if (epi_warp && ep_pend && g >= ep_gl + kStages) {
-          if (!(run = epilogue([&]() {
-                cp_async_wait<0>();
-                land_and_arrive(bar_addr(b->kv_full[pending]));
-                pending = -1;
-              })))
-            break;
-        }
       }
       if (pending >= 0) {
         cp_async_wait<0>();
