@@ -294,6 +294,28 @@ def test_h128_token_counts(B, T):
     compare(out, lse, O, L)
 
 
+def test_h128_short_and_empty_tokens(B):
+    # Persistent clusters walking tokens with no valid slot (every third), one
+    # valid slot, 65 valid slots (a one-slot ragged tile) and full lists: the
+    # per-token Q loads and epilogues across runs of one-tile and empty tokens.
+    cfg = synth.CONFIGS["h128"].with_(T=400, pool=100, seed=47)
+    x = synth.make_inputs(cfg)
+    idx = x["idx"].copy()
+    valid = orc.valid_slots(idx, cfg.num_kv)
+    for t in range(cfg.T):
+        pos = np.flatnonzero(valid[t])
+        if t % 3 == 0:
+            idx[t] = -1
+        elif t % 5 == 1:
+            idx[t, pos[1:]] = -1
+        elif t % 7 == 2:
+            idx[t, pos[65:]] = -1
+    x["idx"] = idx
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
 def _bf16_of(f):
     return synth.bf16_bits(np.asarray(f, np.float32))
 
