@@ -397,7 +397,7 @@ def run_reference(args, cfg) -> None:
         flops += r["flops"]
         secs += r["seconds"]
     value = flops / secs / 1e12
-    sample = (f"{args.steps} steps of {secs / args.steps:.1f} s, {ntok} tokens in all "
+    sample = (f"{args.steps} steps of {secs / args.steps:.3g} s, {ntok} tokens in all "
               f"({ntok // args.steps} per step, consecutive from token {first % cfg.T}, "
               f"wrapping at {cfg.T}) of the {cfg.name} workload (fp64 numpy oracle)")
     line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s",
