@@ -232,12 +232,13 @@ __device__ __forceinline__ void land_and_arrive(uint32_t bar) {
 
 // Warps 0-6 gather every tile together: warp w copies rows w, w+7, ... (lane c
 // copies 16-byte chunk c of each 512-byte half row, one contiguous half row
-// per instruction).  Each warp counts its copies on the stage's barrier once
-// they have landed and been fenced into the async proxy, overlapping them with
-// the next tile's issue only when that tile's stage is already free.  Warp 0
-// also compacts the index lists one token ahead into a double-buffered row
-// list, publishes each token's valid count and loads the token's Q half with
-// 2-D TMA.
+// per instruction).  Each warp counts its copies on the stage's barrier as soon
+// as they have landed and been fenced into the async proxy.  Warp 0 also
+// compacts the index lists one token ahead into a double-buffered row list,
+// publishes each token's valid count, loads Q columns 0-127 of the token's half
+// with 2-D TMA once the previous token's last S has completed (the MMA thread
+// copies them into TMEM and loads columns 128-255) and prefetches the next
+// token's Q into L2.
 template <typename IdxT>
 __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, const CUtensorMap* tm_o,
                               uint8_t* base, Bars* b, uint32_t tmem, uint32_t rank, int warp,
@@ -449,10 +450,14 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
     wait_bar<false, true>(bar_addr(b->q_lo_full), (q_loads - 1) & 1, b, p.err, 1u);
 }
 
-// Warp 3, lane 0: issues every tcgen05.mma of the CTA.
-//   S(g)  = Q_half . K_half(g)^T -> S buffer g%3 (M=128, N=64, K=256: 16 MMAs)
+// Warp 7, lane 0: issues every tcgen05.mma and tcgen05.cp of the CTA.
+//   S(g)  = Q_half . K_half(g)^T -> S buffer g%2 (M=128, N=64, K=256: 16 MMAs,
+//           the first 8 with Q columns 0-127 from TMEM, the last 8 with
+//           columns 128-255 from shared memory)
 //   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs,
 //           P(g) read from TMEM buffer g%2, V from the shared-memory stage)
+// Per token it also copies Q columns 0-127 into TMEM once they have landed and
+// then loads columns 128-255 into the freed buffer.
 // Event-driven: each pass polls (without blocking) whether the next P.V or the
 // next S has its inputs and issues whichever is ready, P.V first because it
 // releases a KV stage.  No operation waits behind another one's inputs.  A
@@ -643,7 +648,7 @@ __device__ __forceinline__ float row_min64(const uint32_t* v) {
 // Warps 8-15: two score warpgroups.  Warpgroup w handles the tiles g with
 // g % 2 == w (tile numbers count every tile of this CTA); thread = TMEM lane =
 // head `row`.  For its tile g a warpgroup
-//   1. reads this CTA's partial scores S_r(g) (64 fp32) from S buffer g%3 and
+//   1. reads this CTA's partial scores S_r(g) (64 fp32) from S buffer g%2 and
 //      frees the buffer; scales them to base-2 logits, takes the row's largest
 //      o_r off and rounds the remainder to fp16;
 //   2. st.asyncs remainder and o_r into the peer's receive buffer g%2 (the
