@@ -20,8 +20,9 @@
 //     rounding of one half's remainder; P, l and the O half of a CTA all come
 //     from the same S, and rank 0 writes lse);
 //   * O[:, half r] += P . V[:, half r] into its own TMEM.
-//   TMEM per CTA: O half 256 columns, two 64-column S buffers, two 32-column
-//   P buffers (bf16 pairs, the A operand of P.V) and the first 128 of the
+//   TMEM per CTA: O half 256 columns, one 64-column S buffer (read out early
+//   by its warpgroup), four 32-column P buffers (bf16 pairs, the A operand of
+//   P.V: each warpgroup's P waits for the P.V two of its tiles back) and the first 128 of the
 //   half's Q columns (64 columns of bf16 pairs, the A operand of the first 8
 //   of S's 16 MMAs; the other 128 Q columns stay in shared memory).  Holding
 //   part of Q in TMEM frees the shared memory for a fourth KV stage: a stage
@@ -81,9 +82,10 @@ constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 4;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 2;
-constexpr uint32_t kTmemS = 256;      // two S buffers (64 columns each); O at 0
-constexpr uint32_t kTmemP = 384;      // two P buffers (32 columns of bf16 pairs each)
+constexpr int kSBufs = 1;
+constexpr int kPBufs = 4;
+constexpr uint32_t kTmemS = 256;      // one S buffer (64 columns); O at 0
+constexpr uint32_t kTmemP = 320;      // four P buffers (32 columns of bf16 pairs each)
 constexpr uint32_t kTmemQ = 448;      // Q columns 0-127 of this CTA's half (64 columns of bf16 pairs)
 
 // shared memory layout (offsets from a 1024-byte aligned base)
@@ -113,13 +115,15 @@ struct Bars {
   uint64_t qcp_done;               // Q columns 0-127 copied into TMEM (MMA commit)
   uint64_t q_empty;                // the token's last S has completed
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[kSBufs];   // partial S(g) in TMEM (MMA commit)
-  uint64_t s_free[kSBufs];   // the score warpgroup has read S(g)
+  // per tile parity (= score warpgroup), so that each barrier completes once per
+  // tile of its warpgroup, in order, although the tiles share one S buffer
+  uint64_t s_full[2];   // partial S(g) in TMEM (MMA commit)
+  uint64_t s_free[2];   // the score warpgroup has read S(g)
   uint64_t m_ready[2][4];    // running max of tile g published (per tile parity, per quadrant)
   uint64_t epi[2];           // both score warpgroups have published their sums (per token
                              // parity: a warpgroup with no tile in a token may already
                              // be done with the next one)
-  uint64_t p_full[2], pv_done[2];   // per P buffer
+  uint64_t p_full[kPBufs], pv_done[kPBufs];   // per P buffer
   uint64_t x_full[kXBufs], x_free[kXBufs];
   uint64_t o_free;
   uint64_t meta_full[2], meta_empty[2];
@@ -276,8 +280,8 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
     const float m_run = fmaxf(m0, m1);   // the max of the token's last tile
     const float l_run = l0 * ex2(m0 - m_run) + l1 * ex2(m1 - m_run);
     // the token's last P.V has completed
-    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[ep_gl & 1]),
-                                                 (ep_gl >> 1) & 1, b, p.err, 1u)))
+    if (!__all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[ep_gl % kPBufs]),
+                                                 (ep_gl / kPBufs) & 1, b, p.err, 1u)))
       return false;
     if (lane == 0) SMLA_TL(3, ep_gl, 5);
     tc_fence_after();
@@ -451,11 +455,11 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
 }
 
 // Warp 7, lane 0: issues every tcgen05.mma and tcgen05.cp of the CTA.
-//   S(g)  = Q_half . K_half(g)^T -> S buffer g%2 (M=128, N=64, K=256: 16 MMAs,
+//   S(g)  = Q_half . K_half(g)^T -> the S buffer (M=128, N=64, K=256: 16 MMAs,
 //           the first 8 with Q columns 0-127 from TMEM, the last 8 with
 //           columns 128-255 from shared memory)
 //   PV(g) : O_half += P(g) . V_half(g)       (M=128, N=256, K=64: 4 MMAs,
-//           P(g) read from TMEM buffer g%2, V from the shared-memory stage)
+//           P(g) read from TMEM buffer g%4, V from the shared-memory stage)
 // Per token it also copies Q columns 0-127 into TMEM once they have landed and
 // then loads columns 128-255 into the freed buffer.
 // Event-driven: each pass polls (without blocking) whether the next P.V or the
@@ -491,13 +495,13 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
     if (pg < sg) {
       const int jj = ring_j[pg % kRing];
       const uint32_t tk = ring_tok[pg % kRing];
-      if (mbar_test_wait(bar_addr(b->p_full[pg & 1]), (pg >> 1) & 1) &&
+      if (mbar_test_wait(bar_addr(b->p_full[pg % kPBufs]), (pg / kPBufs) & 1) &&
           (jj != 0 || mbar_test_wait(bar_addr(b->o_free), (tk & 1) ^ 1))) {
         SMLA_TL(1, pg, 3);
         tc_fence_after();
         const uint32_t s = pg % kStages;
         const uint32_t kv = sbase + kKVOff + s * kStageBytes;
-        const uint32_t ptm = tmem + kTmemP + (pg & 1) * 32;   // P: 64 bf16 = 32 columns
+        const uint32_t ptm = tmem + kTmemP + (pg % kPBufs) * 32;   // P: 64 bf16 = 32 columns
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
           // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart
@@ -505,7 +509,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
           mma_bf16_ts(tmem, ptm + kk * 8, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar_addr(b->kv_empty[s]));
-        mma_commit(bar_addr(b->pv_done[pg & 1]));
+        mma_commit(bar_addr(b->pv_done[pg % kPBufs]));
         SMLA_TL(1, pg, 4);
         ++pg;
         progress = true;
@@ -563,9 +567,11 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
         }
       } else {
         const uint32_t s = sg % kStages, ph = (sg / kStages) & 1;
-        const uint32_t sb = sg % kSBufs, sph = (sg / kSBufs) & 1;
+        const uint32_t sb = sg % kSBufs;
+        // the S buffer's previous tile, S(sg-1), has been read
         if (mbar_test_wait(bar_addr(b->kv_full[s]), ph) &&
-            mbar_test_wait(bar_addr(b->s_free[sb]), sph ^ 1)) {
+            (sg == 0 ||
+             mbar_test_wait(bar_addr(b->s_free[(sg - 1) & 1]), ((sg - 1) >> 1) & 1))) {
           SMLA_TL(1, sg, 1);
           tc_fence_after();
           const uint32_t kv = sbase + kKVOff + s * kStageBytes;
@@ -581,7 +587,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
               mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, 1u);
             }
           }
-          mma_commit(bar_addr(b->s_full[sb]));
+          mma_commit(bar_addr(b->s_full[sg & 1]));
           SMLA_TL(1, sg, 0);
           ring_j[sg % kRing] = j;
           ring_tok[sg % kRing] = tokn;
@@ -648,7 +654,7 @@ __device__ __forceinline__ float row_min64(const uint32_t* v) {
 // Warps 8-15: two score warpgroups.  Warpgroup w handles the tiles g with
 // g % 2 == w (tile numbers count every tile of this CTA); thread = TMEM lane =
 // head `row`.  For its tile g a warpgroup
-//   1. reads this CTA's partial scores S_r(g) (64 fp32) from S buffer g%2 and
+//   1. reads this CTA's partial scores S_r(g) (64 fp32) from the S buffer and
 //      frees the buffer; scales them to base-2 logits, takes the row's largest
 //      o_r off and rounds the remainder to fp16;
 //   2. st.asyncs remainder and o_r into the peer's receive buffer g%2 (the
@@ -659,7 +665,7 @@ __device__ __forceinline__ float row_min64(const uint32_t* v) {
 //      settled for tile g-1 (per row, through shared memory), raises it only
 //      when the tile's max exceeds it by more than 2^8, and publishes it for
 //      tile g+1;
-//   5. writes P = 2^(S - m) (bf16) into TMEM P buffer g%2 and, when the max
+//   5. writes P = 2^(S - m) (bf16) into TMEM P buffer g%4 and, when the max
 //      was raised, first rescales O (after P.V(g-1) has completed).
 // Each warpgroup keeps the sum l of its own tiles (relative to the max it last
 // saw); at the end of a token the two sums are merged through shared memory
@@ -704,10 +710,10 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
     for (int j = 0; j < ntiles; ++j) {
       const uint32_t g = gt + j;
       if (static_cast<int>(g & 1u) != wg) continue;
-      const uint32_t sb = g % kSBufs, xb = g % kXBufs, pb = g & 1;
+      const uint32_t sb = g % kSBufs, xb = g % kXBufs, pb = g % kPBufs;
       // 1. my partial scores, rounded to fp16; the S buffer is free again
-      if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[sb]),
-                                                         (g / kSBufs) & 1, b, p.err, 8u))))
+      if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->s_full[g & 1]),
+                                                         (g >> 1) & 1, b, p.err, 8u))))
         break;
       if (row == 0) SMLA_TL(2, g, 0);
       tc_fence_after();
@@ -721,7 +727,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
         tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar_addr(b->s_free[sb]));
+        mbar_arrive(bar_addr(b->s_free[g & 1]));
         // the row's top partial in base-2 logits over the valid columns (rounding
         // is monotone, so the extreme raw value scales to the largest scaled one;
         // a negative scale turns the smallest raw value into it).  The zero-filled
@@ -824,16 +830,17 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
       const float2 sa = add2(add2(sum4[0], sum4[1]), add2(sum4[2], sum4[3]));
       l_w = l_w * ex2(m_lw - m_new) + (sa.x + sa.y);
       m_lw = m_new;
-      // P buffer pb was last read by P.V(g-2); O may only be rescaled after P.V(g-1)
-      if (g >= 2) {
+      // P buffer pb was last read by P.V(g-4); O may only be rescaled after P.V(g-1)
+      if (g >= kPBufs) {
         if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb]),
-                                                           ((g >> 1) & 1) ^ 1, b, p.err, 4u))))
+                                                           ((g / kPBufs) & 1) ^ 1, b, p.err, 4u))))
           break;
         tc_fence_after();
       }
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->pv_done[pb ^ 1]),
-                                                           ((g - 1) >> 1) & 1, b, p.err, 4u))))
+        if (!(ok = __all_sync(0xffffffffu,
+                              wait_bar<false>(bar_addr(b->pv_done[(g - 1) % kPBufs]),
+                                              ((g - 1) / kPBufs) & 1, b, p.err, 4u))))
           break;
         tc_fence_after();
         const float alpha = ex2(m_prev - m_new);   // 1 for rows whose max stayed
@@ -893,16 +900,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_addr(b->kv_full[s]), kProducerThreads);
       mbar_init(bar_addr(b->kv_empty[s]), 1);
     }
-    for (int i = 0; i < kSBufs; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->s_full[i]), 1);
       mbar_init(bar_addr(b->s_free[i]), kWgThreads);
     }
     for (int i = 0; i < 2; ++i)
       for (int q = 0; q < 4; ++q) mbar_init(bar_addr(b->m_ready[i][q]), 32);
     for (int i = 0; i < 2; ++i) mbar_init(bar_addr(b->epi[i]), 2 * kWgThreads);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPBufs; ++i) {
       mbar_init(bar_addr(b->p_full[i]), kWgThreads);
       mbar_init(bar_addr(b->pv_done[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->meta_full[i]), 1);
       mbar_init(bar_addr(b->meta_empty[i]), 1 + 2 * kWgThreads);
     }
