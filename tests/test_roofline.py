@@ -40,3 +40,34 @@ def test_terms_pick_the_slower_term():
     assert abs(t["gathered"]["time_s"] - 0.270e-3 - 0.16e-3) < 0.01e-3
     assert t["roofline_gathered_s"] == max(t["flop"]["time_s"], t["gathered"]["time_s"])
     assert abs(t["frac_of_roofline_gathered"] - t["roofline_gathered_s"] / 1e-3) < 1e-12
+
+
+def _bench_module():
+    import importlib.util
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(root, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_committed_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
+    # The bench reports an ncu DRAM traffic figure only from a summary taken on
+    # the kernel source it runs (same sha256 prefix), and null otherwise.
+    b = _bench_module()
+    src = tmp_path / "sparse_mla_attention_token_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "smla_h128.cu").write_text("// kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    assert b.committed_traffic(1, "h128") == (None, "no ncu summary for this kernel/workload")
+    sha = b.kernel_source_sha(1)
+    (tmp_path / "profiles" / "k.md").write_text(
+        f"traffic_per_launch: kernel=h128_fwd_kernel workload=h128 source_sha={sha} "
+        f"dram_bytes=12345\n")
+    assert b.committed_traffic(1, "h128") == (12345, "profiles/k.md")
+    assert b.committed_traffic(1, "h128_long")[0] is None
+    (src / "smla_h128.cu").write_text("// kernel v2\n")
+    v, why = b.committed_traffic(1, "h128")
+    assert v is None and "another source" in why
