@@ -427,13 +427,13 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
         }
         cp_async_commit();
         if (lane == 0) SMLA_TL(0, g, 1);
-        if (!compacted && j == ntiles - 1) compact_next();   // overlaps the copies
         // count this tile as soon as its copies have landed: the MMA waits for the
         // slowest warp, so counting it after the next tile's issue (overlapping
         // the two) made every tile ready later (2% slower overall)
         cp_async_wait<0>();
         land_and_arrive(bar_addr(b->kv_full[s]));
         if (lane == 0) SMLA_TL(0, g, 2);
+        if (!compacted && j == ntiles - 1) compact_next();   // after counting the tile
       }
       gt += ntiles;
       if (epi_warp && run) {   // epilogues run in token order
