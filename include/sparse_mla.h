@@ -19,9 +19,9 @@
  *   A duplicated row counts once per slot that names it.
  *
  * Numerics: S and the softmax run in fp32 (base 2, scale folded into one
- * multiply); the probabilities P are rounded to bf16 before P.V, as the
- * reference's bf16 dot does; O is accumulated in fp32 and rounded to bf16
- * once.  The H = 128 kernel splits the 512-wide contraction between the two
+ * multiply); the probabilities P are rounded to bf16 before P.V (a choice
+ * the definition above leaves open); O is accumulated in fp32 and rounded to
+ * bf16 once.  The H = 128 kernel splits the 512-wide contraction between the two
  * CTAs of a cluster: each takes its row's largest partial score off, rounds
  * the remainder it sends to the other CTA to fp16 and adds the received one to
  * its own in fp32, so a score's error is at most 2^-11 of how far its partial
