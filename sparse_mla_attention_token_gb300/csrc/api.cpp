@@ -216,14 +216,26 @@ cudaError_t host_streams(HostStreams** out, std::unique_lock<std::mutex>* lock) 
   *lock = std::unique_lock<std::mutex>(mu);
   HostStreams& h = per_dev[dev];
   if (!h.ready) {
-    if ((e = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
     const unsigned f = cudaEventDisableTiming;
-    if ((e = cudaEventCreateWithFlags(&h.start, f)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&h.done, f)) != cudaSuccess) return e;
-    for (int i = 0; i < kMaxHostChunks; ++i) {
-      if ((e = cudaEventCreateWithFlags(&h.in_ev[i], f)) != cudaSuccess) return e;
-      if ((e = cudaEventCreateWithFlags(&h.k_ev[i], f)) != cudaSuccess) return e;
+    e = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, f);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.done, f);
+    for (int i = 0; i < kMaxHostChunks && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&h.in_ev[i], f);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.k_ev[i], f);
+    }
+    if (e != cudaSuccess) {   // release what was made, so that a later call starts afresh
+      if (h.in) cudaStreamDestroy(h.in);
+      if (h.out) cudaStreamDestroy(h.out);
+      if (h.start) cudaEventDestroy(h.start);
+      if (h.done) cudaEventDestroy(h.done);
+      for (int i = 0; i < kMaxHostChunks; ++i) {
+        if (h.in_ev[i]) cudaEventDestroy(h.in_ev[i]);
+        if (h.k_ev[i]) cudaEventDestroy(h.k_ev[i]);
+      }
+      h = HostStreams{};
+      return e;
     }
     h.ready = true;
   }
