@@ -53,3 +53,16 @@ def test_golden_catches_planted_mistake(kind, monkeypatch):
         except Exception:
             caught.append(True)
     assert any(caught), f"golden fixtures miss the planted mistake {kind!r}"
+
+
+@pytest.mark.parametrize("name", fixtures.NAMES)
+def test_fixture_file_is_what_its_generator_writes(name):
+    """The stored JSON is exactly the closed-form generator's output (no hand edits)."""
+    pytest.importorskip("mpmath")
+    import json
+    import os
+    from tests.golden import make_golden
+    fx = getattr(make_golden, name)()
+    with open(os.path.join(os.path.dirname(make_golden.__file__), name + ".json")) as f:
+        stored = json.load(f)
+    assert json.loads(json.dumps(fx)) == stored
