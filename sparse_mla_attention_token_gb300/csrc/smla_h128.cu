@@ -350,6 +350,13 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
     if (b->prod_stop) break;
     const int nv = b->prod_nv[buf];
     const int* rows = rows_buf + buf * kMaxTopk;
+    if (warp == 0 && tok + ncl < p.T) {
+      // the next token's index row into L2: warp 0 compacts it at the end of
+      // this token, on the way to the next token's first gather
+      const int64_t bytes = int64_t(p.topk) * int64_t(sizeof(IdxT));
+      const char* ip = static_cast<const char*>(p.idx) + (tok + ncl) * bytes;
+      for (int64_t o = int64_t(lane) * 128; o < bytes; o += 32 * 128) prefetch_l2(ip + o);
+    }
     if (warp == 0) {
       const int slot = it & 1;
       bool ok = __all_sync(0xffffffffu, wait_bar<false>(bar_addr(b->meta_empty[slot]),
