@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config h128] [--e2e-steps E] [--cpu-seconds S]
+                    [--per-workload all|none|name,name,...] [--pw-steps P]
 
 A step is one forward call over the whole workload (all tokens of the
 configuration; default the T=4096 H=128 topk=512 workload the headline metric
@@ -14,6 +15,13 @@ K steps, max over ranks.
 Under torchrun (N > 1) every rank runs its own seeded batch of the workload on
 its own GPU (weak scaling, no collective on the data path); ``value`` is the
 FLOPs of all ranks over the slowest rank's time.
+
+Besides the headline workload, the JSON line carries ``per_workload``: every
+other workload (the small-head workload, the H=8 top-k sweep with the sink on
+and off, the long H=128 workload, the GLM-shaped top-k 2048 call, the tiny
+workload and decode-sized calls of 1-16 tokens), each timed the same way (L2
+flushed before every timed call, CUDA events on the launching stream), with
+its roofline fractions and the fp64 oracle timed on a bounded token sample.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this op
 has) on bounded token samples of the same workload, on rank 0 only.
@@ -224,6 +232,81 @@ def _device_inputs(x, cfg, dev):
     return q, kv, idx, sink, keep
 
 
+# Workloads reported beside the headline, in this order.
+PER_WORKLOAD = ["small_head", "sweep_k32", "sweep_k32_nosink", "sweep_k128", "sweep_k128_nosink",
+                "sweep_k256", "sweep_k256_nosink", "sweep_k640", "sweep_k640_nosink", "h128_long",
+                "glm_k2048", "tiny", "decode_h8_t1", "decode_h8_t4", "decode_h8_t16",
+                "decode_h16_t1", "decode_h16_t4", "decode_h16_t16", "decode_h128_t1",
+                "decode_h128_t4", "decode_h128_t16"]
+
+
+def time_calls(fn, steps: int, warmup: int, flush, stream) -> list:
+    """Per-call device times (ms) of ``fn``: L2 flushed before every call, CUDA
+    events recorded on ``stream`` around the call only."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def measure_workload(name: str, args, dev, flush, stream, peaks: dict) -> dict:
+    """One per-workload entry: device time per call, roofline, oracle baseline."""
+    import torch
+    from sparse_mla_attention_token_gb300 import binding as B
+    cfg = synth.CONFIGS[name]
+    x = synth.make_inputs(cfg)
+    counts = roofline.count(x["idx"], cfg.num_kv, cfg.H, cfg.sink)
+    q, kv, idx, sink, keep = _device_inputs(x, cfg, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device=dev)
+    family, splits, launches = B.sparse_mla_plan(cfg.T, cfg.H, cfg.topk)
+
+    def step():
+        B.sparse_mla_fwd(q, kv, idx, sink, x["scale"], out=out, lse=lse)
+
+    ms = time_calls(step, args.pw_steps, 3, flush, stream)
+    if B.sparse_mla_device_status() != 0:
+        raise RuntimeError(f"device status not OK after {name}")
+    med = statistics.median(ms)
+    t = roofline.terms(counts, med * 1e-3, peaks)
+    e = {"workload": workload_desc(cfg), "kernel": KERNEL_NAMES[family],
+         "kernel_family": family, "splits": splits, "launches_per_call": launches,
+         "ms_per_call": med, "ms_min": min(ms), "ms_max": max(ms), "steps": len(ms),
+         "tflops": counts.flops / (med * 1e-3) / 1e12,
+         "valid_slots": counts.valid, "unique_rows": counts.unique_rows,
+         "bound": "tensor" if t["flop"]["time_s"] >= t["gathered"]["time_s"] else "hbm",
+         "frac_of_roofline_gathered": t["frac_of_roofline_gathered"],
+         "frac_of_roofline_unique": t["frac_of_roofline_unique"],
+         "tensor_frac": t["flop"]["frac"],
+         "roofline_gathered_ms": t["roofline_gathered_s"] * 1e3,
+         "roofline_unique_ms": t["roofline_unique_s"] * 1e3,
+         "gpu_launches": len(ms) * launches}
+    if cfg.T <= 16:
+        # decode-sized calls are latency-bound: the device time of one tiny kernel
+        # launch (a 1-element fill, same events, same stream) is their floor
+        one = flush[:1]
+        floor = time_calls(lambda: one.zero_(), args.pw_steps, 3, flush, stream)
+        e["launch_floor_ms"] = statistics.median(floor)
+    if args.cpu_seconds > 0:
+        r = oracle_rate(x, cfg, min(args.cpu_seconds, 2.0))
+        e["cpu_baseline"] = {
+            "value": r["tflops"], "unit": "TFLOP/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"tokens {r['first_token']}..{r['first_token'] + r['tokens'] - 1} "
+                      f"({r['tokens']} tokens, {r['seconds']:.2f} s, fp64 numpy oracle)"}
+    del q, kv, idx, sink, keep, out, lse
+    return e
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, cfg) -> None:
     import torch
@@ -361,6 +444,20 @@ def run_ours(args, cfg) -> None:
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
                         "max": max(step_ms),
                         "warm_l2_median": statistics.median(warm_ms) if warm_ms else None}}
+    if args.per_workload != "none" and world == 1:
+        names = PER_WORKLOAD if args.per_workload == "all" else args.per_workload.split(",")
+        pw = {}
+        pw_sampler = ClockSampler(_physical_gpu(local_rank))
+        pw_sampler.start()
+        p0 = time.time()
+        for n in names:
+            if n == cfg.name:
+                continue
+            pw[n] = measure_workload(n, args, dev, flush, stream, peaks)
+            torch.cuda.empty_cache()
+        pw_sampler.mark(p0, time.time())
+        line["per_workload"] = pw
+        line["per_workload_clocks"] = pw_sampler.stop()
     if world == 1 and rank == 0 and args.cpu_seconds > 0:
         r = oracle_rate(x, cfg, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -423,6 +520,10 @@ def main(argv=None) -> int:
     ap.add_argument("--config", default=synth.BENCH_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--per-workload", default="all",
+                    help="other workloads to report: all, none, or a comma-separated list")
+    ap.add_argument("--pw-steps", type=int, default=20,
+                    help="timed calls per workload in per_workload")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="total seconds of oracle work for --impl reference")
     args = ap.parse_args(argv)

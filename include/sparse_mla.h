@@ -101,13 +101,19 @@ smla_status_t sparse_mla_fwd(const void* q, const void* kv, const void* topk_ind
  * sparse_mla_fwd_ex -- sparse_mla_fwd with two test/benchmark controls.
  *
  *   num_splits   0 = library choice; otherwise 1..64: the topk slots of each
- *                token are cut into num_splits contiguous ranges computed
- *                independently and merged by a combine kernel (the
- *                split-TOPK path; lse-weighted merge, the sink folded once).
- *   read_trace   NULL, or a device int64 [T, topk] buffer: the kernel writes,
- *                for every slot, the kv row it gathers for that slot, or -1
- *                when the slot is invalid and nothing is read.  Written by
- *                the same code that forms the gather address.
+ *                token are cut into num_splits contiguous ranges of
+ *                ceil(topk / num_splits) slots, computed independently and
+ *                merged by a combine kernel (the split-TOPK path;
+ *                lse-weighted merge, the sink folded once).
+ *   read_trace   NULL, or a device int64 [T, topk] buffer that records which
+ *                kv rows the kernel's copies read.  Per token and per slot
+ *                range (one range when the call does not split), the entries
+ *                hold, in order, the row each gather reads for the range's
+ *                valid slots (slot order; a duplicated row appears once per
+ *                slot), then -1 for the rest of the range.  Each row entry is
+ *                recovered from the source address of the copy that reads it,
+ *                where that address is formed; the -1 entries are written
+ *                where the slots are classified (nothing is read for them).
  */
 smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_indices,
                                 int32_t index_dtype, const float* attn_sink, float scale,
@@ -119,13 +125,14 @@ smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_
  * sparse_mla_fwd_static_scratch -- the split-TOPK path without any allocation.
  *
  * The pages have no counterpart to this entry point.  It exists for callers
- * that must not allocate device memory while they run: code executing under a
- * CUDA stream capture that must not add allocation nodes, serving loops with a
+ * that must not allocate device memory while they run: code recorded into a
+ * stream capture that must not contain allocation steps, serving loops with a
  * fixed memory budget, and hosts whose allocator is owned by another runtime.
  * sparse_mla_fwd_ex allocates the split path's partial results on every call;
  * this entry point keeps them in one fixed array inside the library instead
- * (16 MiB of device memory, held by every GPU that loads the library until the
- * process exits) and calls no cudaMalloc / cudaFree or any allocating routine.
+ * (8192 x 2052 bytes = 16,809,984 bytes of device memory, held by every GPU
+ * that loads the library until the process exits) and calls no cudaMalloc /
+ * cudaFree or any allocating routine.
  *
  *   Arguments and results: as sparse_mla_fwd (same layouts, same validation).
  *   num_splits   0 = the library's split count (at least 2); otherwise 2..64.
@@ -133,8 +140,12 @@ smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_
  *                SMLA_ERR_SCRATCH_LIMIT before any CUDA call.  This suits
  *                decode-sized calls (a few tokens); larger calls belong on
  *                sparse_mla_fwd.
- *   First call   on each device looks up the array's device address once;
- *                make it before any stream capture.
+ *   First call   on each device (and again after that device's context has
+ *                been reset) looks up the array's device address.  With CUDA's
+ *                lazy module loading that lookup is what loads the library's
+ *                device code and maps the array, an allocation made by the
+ *                driver: make the first call before any stream capture and
+ *                outside any no-allocation window.
  *   Sharing      every call uses the same array: calls whose kernels overlap
  *                on the GPU (other streams, other host threads) race and give
  *                wrong results.  Serialise them on one stream.  No state
@@ -194,9 +205,12 @@ smla_status_t sparse_mla_fwd_host_workspace(int64_t T, int32_t H, int32_t topk, 
 
 /*
  * sparse_mla_plan -- what sparse_mla_fwd_ex would launch, without launching.
- * Host only (no CUDA call).  Writes the kernel family (0 = small-head kernel,
- * 1 = tcgen05 H=128 kernel), the split count and the number of kernel
- * launches per call.  num_splits as in sparse_mla_fwd_ex.
+ * Launches nothing and touches no memory; its one CUDA query is the current
+ * device's SM count (looked up once per device), which the split count
+ * depends on (152 SMs are assumed when no device can be queried).  Writes the
+ * kernel family (0 = small-head kernel, 1 = tcgen05 H=128 kernel), the split
+ * count and the number of kernel launches per call.  num_splits as in
+ * sparse_mla_fwd_ex.
  */
 smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_splits,
                               int32_t* kernel_family, int32_t* splits_out,

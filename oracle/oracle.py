@@ -69,12 +69,15 @@ def token_forward(q_t: np.ndarray, kv: np.ndarray, idx_t: np.ndarray, num_kv: in
                   sink, scale: float):
     """One token: returns (O [H, D] float64, lse [H] float64).
 
-    ``q_t`` is float64 ``[H, D]``, ``kv`` float64 ``[num_kv, D]``, ``sink`` a
+    ``q_t`` is float64 ``[H, D]``, ``kv`` ``[num_kv, D]`` either float64 or
+    bf16 bit patterns (uint16, widened exactly after the gather), ``sink`` a
     float64 ``[H]`` array or None.
     """
     H, D = q_t.shape
     rows = np.asarray(idx_t).astype(np.int64)[valid_slots(idx_t, num_kv)]
     k = kv[rows]                                   # [v, D]; a duplicated row appears twice
+    if k.dtype == np.uint16:
+        k = bf16_to_f64(k)
     s = scale * (q_t @ k.T)                        # [H, v]
     m = s.max(axis=1) if rows.size else np.full(H, -np.inf)
     if sink is not None:
@@ -103,7 +106,7 @@ def sparse_mla_fwd(q_bits: np.ndarray, kv_bits: np.ndarray, idx: np.ndarray, sin
     Returns (O float64 ``[n, H, D]``, lse float64 ``[n, H]``) for those tokens.
     """
     num_kv = kv_bits.shape[0]
-    kv = bf16_to_f64(kv_bits)
+    kv = np.asarray(kv_bits, dtype=np.uint16)      # rows are widened once gathered
     sk = None if sink is None else np.asarray(sink, dtype=np.float32).astype(np.float64)
     T, H, D = q_bits.shape
     toks = range(T) if tokens is None else list(tokens)

@@ -24,7 +24,7 @@ namespace {
 
 constexpr int32_t kAbiVersion = 1;
 constexpr int kMaxSplits = 64;
-constexpr int kNumSMs = 152;  // GB300; only used to pick a split count
+constexpr int kDefaultSMs = 152;  // planning without a device (host-only checks)
 
 thread_local char g_last_cuda_error[256] = "";
 
@@ -48,8 +48,30 @@ struct Plan {
   int launches;
 };
 
+// Streaming multiprocessors of the current device (looked up once per device),
+// or kDefaultSMs when no device can be queried.
+int device_sms() {
+  static int per_dev[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();   // no device here: clear the error and plan for the default
+    return kDefaultSMs;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (per_dev[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return kDefaultSMs;
+    }
+    per_dev[dev] = n;
+  }
+  return per_dev[dev];
+}
+
 smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int64_t num_kv, int32_t num_splits,
-                        Plan* pl) {
+                        int num_sms, Plan* pl) {
   if (num_splits < 0 || num_splits > kMaxSplits) return SMLA_ERR_BAD_SPLITS;
   const int min_splits =
       std::max(1, (topk + smla::kSmallHMaxSlots - 1) / smla::kSmallHMaxSlots);
@@ -62,8 +84,8 @@ smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int64_t num_kv, int3
     // enough CTAs to cover the GPU twice; each split keeps >= 64 slots
     const int64_t ctas = T * ((H + 15) / 16);
     splits = 1;
-    if (ctas > 0 && ctas < 2 * kNumSMs) {
-      const int64_t want = (2 * kNumSMs + ctas - 1) / ctas;
+    if (ctas > 0 && ctas < 2 * num_sms) {
+      const int64_t want = (2 * num_sms + ctas - 1) / ctas;
       splits = static_cast<int>(std::min<int64_t>(want, std::max(1, topk / 64)));
       splits = std::min(splits, 16);
     }
@@ -121,7 +143,7 @@ smla_status_t run(const void* q, const void* kv, const void* idx, int32_t index_
       validate(q, kv, idx, index_dtype, sink, scale, out, lse, T, H, num_kv, topk, trace);
   if (st != SMLA_OK) return st;
   Plan pl;
-  st = make_plan(T, H, topk, num_kv, num_splits, &pl);
+  st = make_plan(T, H, topk, num_kv, num_splits, T > 0 ? device_sms() : kDefaultSMs, &pl);
   if (st != SMLA_OK) return st;
   if (T == 0) return SMLA_OK;
 
@@ -269,7 +291,7 @@ smla_status_t sparse_mla_fwd_host(const void* q_host, const void* kv_host,
                               scale, out_host, lse_host, T, H, num_kv, topk, nullptr);
   if (st != SMLA_OK) return st;
   Plan pl;
-  st = make_plan(T, H, topk, num_kv, 0, &pl);
+  st = make_plan(T, H, topk, num_kv, 0, T > 0 ? device_sms() : kDefaultSMs, &pl);
   if (st != SMLA_OK) return st;
   if (T == 0) return SMLA_OK;
   const HostWs w = host_ws_layout(T, H, topk, num_kv, index_dtype, attn_sink_host != nullptr);
@@ -367,7 +389,7 @@ smla_status_t sparse_mla_fwd_static_scratch(const void* q, const void* kv,
   if (st != SMLA_OK) return st;
   if (num_splits == 1) return SMLA_ERR_BAD_SPLITS;   // this path always splits
   Plan pl;
-  st = make_plan(T, H, topk, num_kv, num_splits, &pl);
+  st = make_plan(T, H, topk, num_kv, num_splits, T > 0 ? device_sms() : kDefaultSMs, &pl);
   if (st != SMLA_OK) return st;
   const int splits = std::max(2, pl.splits);
   if (T == 0) return SMLA_OK;
@@ -398,7 +420,7 @@ smla_status_t sparse_mla_plan(int64_t T, int32_t H, int32_t topk, int32_t num_sp
   if (T < 0 || topk < 0) return SMLA_ERR_BAD_SHAPE;
   if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
   Plan pl;
-  const smla_status_t st = make_plan(T, H, topk, 1, num_splits, &pl);
+  const smla_status_t st = make_plan(T, H, topk, 1, num_splits, device_sms(), &pl);
   if (st != SMLA_OK) return st;
   if (kernel_family) *kernel_family = pl.family;
   if (splits_out) *splits_out = pl.splits;
@@ -413,7 +435,7 @@ smla_status_t sparse_mla_launch_config(int64_t T, int32_t H, int32_t topk, int64
   if (T < 0 || topk < 0 || num_kv < 0) return SMLA_ERR_BAD_SHAPE;
   if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
   Plan pl;
-  smla_status_t st = make_plan(T, H, topk, num_kv, num_splits, &pl);
+  smla_status_t st = make_plan(T, H, topk, num_kv, num_splits, device_sms(), &pl);
   if (st != SMLA_OK) return st;
   smla::LaunchGeom g{0, 0, 0, 0};
   const int e = pl.family == 1 ? smla::h128_geometry(T, &g)

@@ -198,7 +198,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Bars* b,
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t& b) { return smem_u32(&b); }
 
 // Compact one token's valid slots (slot order) into `rows`; returns the count.
-// Warp-collective (warp 0).  Loads are issued kUnroll deep before use.
+// Warp-collective (warp 0).  Loads are issued kUnroll deep before use.  With a
+// read trace, the entries past the token's valid count are set to -1 here (no
+// copy ever reads for them); the gather writes the others.
 template <typename IdxT>
 __device__ __forceinline__ int compact_token(const H128Params& p, int64_t tok, int* rows,
                                              bool write_trace, int lane) {
@@ -216,13 +218,13 @@ __device__ __forceinline__ int compact_token(const H128Params& p, int64_t tok, i
     for (int u = 0; u < kUnroll; ++u) {
       const int j = base + u * 32 + lane;
       const bool ok = (j < p.topk) && slot_valid<IdxT>(v[u], p.num_kv);
-      const int row = ok ? static_cast<int>(v[u]) : -1;   // exact: num_kv < 2^31
       const unsigned ball = __ballot_sync(0xffffffffu, ok);
-      if (ok) rows[nv + __popc(ball & ((1u << lane) - 1u))] = row;
-      if (write_trace && j < p.topk) p.trace[tok * p.topk + j] = row;
+      if (ok) rows[nv + __popc(ball & ((1u << lane) - 1u))] = static_cast<int>(v[u]);  // exact: num_kv < 2^31
       nv += __popc(ball);
     }
   }
+  if (write_trace)
+    for (int k = nv + lane; k < p.topk; k += 32) p.trace[tok * p.topk + k] = -1;
   __syncwarp();
   return nv;
 }
@@ -430,6 +432,9 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
             const bool valid = rr >= 0;                // the ragged tail is zero-filled
             const char* src = valid ? kvb + int64_t(rr) * 1024 + c * 16 : kvb;
             cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+            // read trace: the row this copy reads, recovered from its source address
+            if (trace && c == 0 && valid)
+              p.trace[tok * p.topk + j * kTileN + r] = (src - kvb) >> 10;
           }
         }
         cp_async_commit();

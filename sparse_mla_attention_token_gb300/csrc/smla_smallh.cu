@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
         const IdxT x = idx[j];
         v = slot_valid<IdxT>(x, p.num_kv);
         if (v) row = static_cast<int>(x);   // exact: num_kv < 2^31
-        if (p.trace != nullptr && hg == 0) p.trace[t * p.topk + j] = v ? row : -1;
       }
       const unsigned ball = __ballot_sync(0xffffffffu, v);
       if (lane == 0) sm.warp_cnt[warp] = __popc(ball);
@@ -139,12 +138,16 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
       nvalid += total;
       __syncthreads();
     }
+    // read trace: the range's entries past its valid count are never read (-1);
+    // the gather writes the others
+    if (p.trace != nullptr && hg == 0)
+      for (int k = j0 + nvalid + tid; k < j1; k += kThreads) p.trace[t * p.topk + k] = -1;
     return nvalid;
   };
 
   const char* kvb = static_cast<const char*>(p.kv);
-  // gather tile `tile` of the rows in list `buf` (count nvalid) into `stage`
-  auto issue_tile = [&](int buf, int nvalid, int tile, int stage) {
+  // gather tile `tile` of token t's rows in list `buf` (count nvalid) into `stage`
+  auto issue_tile = [&](int64_t t, int buf, int nvalid, int tile, int stage) {
     const uint32_t dst0 = smem_u32(sm.kv[stage]);
     const int* rows = sm.rows[buf];
 #pragma unroll 4
@@ -154,6 +157,9 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
       const bool ok = slot < nvalid;
       const char* src = ok ? kvb + int64_t(rows[slot]) * kRowBytes + c * 16 : kvb;
       cp_async_16(kv_chunk_addr(dst0, r, c), src, ok ? 16u : 0u);
+      // read trace: the row this copy reads, recovered from its source address
+      if (p.trace != nullptr && hg == 0 && c == 0 && ok)
+        p.trace[t * p.topk + j0 + slot] = (src - kvb) / kRowBytes;
     }
     cp_async_commit();
   };
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
   int cur = 0;                    // row list of the current token
   int nv_cur = compact(t0, cur);
   uint32_t gt = 0;                // tiles issued before the current one (stage = gt & 1)
-  if (nv_cur > 0) issue_tile(cur, nv_cur, 0, 0);
+  if (nv_cur > 0) issue_tile(t0, cur, nv_cur, 0, 0);
 
   for (int64_t t = t0; t < p.T; t += tstride) {
     const int64_t tn = t + tstride;
@@ -187,11 +193,11 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
       cp_async_wait<0>();
       __syncthreads();  // tile `it` landed; every warp is done with the other stage
       if (it + 1 < ntiles) {
-        issue_tile(cur, nv_cur, it + 1, stage ^ 1);
+        issue_tile(t, cur, nv_cur, it + 1, stage ^ 1);
       } else if (tn < p.T) {
         nv_next = compact(tn, cur ^ 1);
         next_done = true;
-        if (nv_next > 0) issue_tile(cur ^ 1, nv_next, 0, stage ^ 1);
+        if (nv_next > 0) issue_tile(tn, cur ^ 1, nv_next, 0, stage ^ 1);
       }
       const uint32_t kvs = smem_u32(sm.kv[stage]);
       // ---- 3. partial S over this warp's 64 columns
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
     if (tn < p.T) {
       if (!next_done) {
         nv_next = compact(tn, cur ^ 1);
-        if (nv_next > 0) issue_tile(cur ^ 1, nv_next, 0, gt & 1);
+        if (nv_next > 0) issue_tile(tn, cur ^ 1, nv_next, 0, gt & 1);
       }
       load_q(tn);
     }

@@ -31,15 +31,24 @@ from typing import Optional
 import numpy as np
 
 D = 512
+NAN_BITS = 0x7FC0   # a bf16 quiet NaN
 
 
 @dataclasses.dataclass(frozen=True)
 class Config:
     """One synthetic workload.
 
-    ``num_kv = T + pool``: kv rows ``0..T-1`` are per-token rows and
-    ``T..num_kv-1`` the compressed pool (kv layout of the "Contract" section of
-    "Sparse MLA training backward").
+    Without ``pos0``/``base_row``, ``num_kv = T + pool``: kv rows ``0..T-1``
+    are per-token rows and ``T..num_kv-1`` the compressed pool (kv layout of
+    the "Contract" section of "Sparse MLA training backward").
+
+    ``pos0`` places the T query tokens at positions ``pos0 .. pos0+T-1`` of a
+    longer sequence (a decode-sized call: the last few tokens of a long
+    context), so the sequence has ``ctx = pos0 + T`` token rows.  ``base_row``
+    puts the sequence's rows at ``base_row ..`` of a shared pool whose first
+    ``base_row`` rows belong to other sequences: no slot names them, and they
+    hold a NaN pattern so that a read of one would show in the output.
+    In general ``num_kv = base_row + ctx + pool``.
     """
 
     name: str
@@ -53,10 +62,17 @@ class Config:
     sink: bool = True
     kv_offset_bytes: int = 0  # where kv starts inside its device allocation
     seed: int = 0
+    pos0: int = 0             # position of query token 0 in its sequence
+    base_row: int = 0         # first kv row of this sequence in a shared pool
+
+    @property
+    def ctx(self) -> int:
+        """Token rows of the sequence (the context up to the last query token)."""
+        return self.pos0 + self.T
 
     @property
     def num_kv(self) -> int:
-        return self.T + self.pool
+        return self.base_row + self.ctx + self.pool
 
     @property
     def scale(self) -> float:
@@ -84,13 +100,39 @@ CONFIGS = {
                          seed=2),
     "sweep_k640_nosink": Config("sweep_k640_nosink", T=4096, H=8, pool=1024, ratio=4, topk=640,
                                 window=128, sink=False, seed=2),
+    "sweep_k32_nosink": Config("sweep_k32_nosink", T=4096, H=8, pool=1024, ratio=4, topk=32,
+                               window=32, sink=False, seed=2),
+    "sweep_k128_nosink": Config("sweep_k128_nosink", T=4096, H=8, pool=1024, ratio=4, topk=128,
+                                window=128, sink=False, seed=2),
+    "sweep_k256_nosink": Config("sweep_k256_nosink", T=4096, H=8, pool=1024, ratio=4, topk=256,
+                                window=128, sink=False, seed=2),
     "h128": Config("h128", T=4096, H=128, pool=1024, ratio=4, topk=512, window=128, seed=3),
     "h128_long": Config("h128_long", T=8192, H=128, pool=1024, ratio=8, topk=1024, window=256,
                         index_dtype="int64", kv_offset_bytes=(2 << 30) + 4096, seed=4),
     # the h128 recipe at a quarter of the tokens: the small case for Nsight Compute captures
     "h128_small": Config("h128_small", T=1024, H=128, pool=256, ratio=4, topk=512, window=128,
                          seed=3),
+    # The GLM-shaped call of "Tuned sparse MLA prefill for DSv4.1-Flash TP4" (review
+    # thread: 16 heads per rank, D=512, top-k 2048, a 16K-row call, a KV pool over
+    # 2 GiB): the sequence's rows start 2^21 rows (2 GiB) into the pool, so every
+    # row it names lies beyond a 32-bit byte offset.
+    "glm_k2048": Config("glm_k2048", T=16384, H=16, pool=4096, ratio=4, topk=2048, window=128,
+                        base_row=1 << 21, seed=5),
 }
+
+# Decode-sized calls: the last T tokens of an 8192-token context ("Tuned sparse
+# MLA prefill for DSv4.1-Flash TP4", review note on 2-16-row calls), with the
+# per-rank head counts 8/16 (640 slots: window 128 + 512 pool) and H = 128
+# (512 slots: window 128 + 384 pool); pool ratio 4.
+DECODE_T = (1, 2, 4, 8, 16)
+DECODE_H = (8, 16, 128)
+for _h in DECODE_H:
+    for _t in DECODE_T:
+        _k = 512 if _h == 128 else 640
+        CONFIGS[f"decode_h{_h}_t{_t}"] = Config(
+            f"decode_h{_h}_t{_t}", T=_t, H=_h, pool=2048, ratio=4, topk=_k, window=128,
+            pos0=8192 - _t, seed=100 + 10 * _h + _t)
+del _h, _t, _k
 
 # The workload the headline metric is quoted on (T=4096 H=128 topk=512).
 BENCH_CONFIG = "h128"
@@ -128,18 +170,19 @@ def make_indices(cfg: Config, rng: np.random.Generator) -> np.ndarray:
         raise ValueError("window larger than TOPK")
     dt = np.int64 if cfg.index_dtype == "int64" else np.int32
     idx = np.full((T, K), -1, dtype=np.int64)
-    t = np.arange(T, dtype=np.int64)
+    t = cfg.pos0 + np.arange(T, dtype=np.int64)       # positions in the sequence
     # window segment: rows t-W+1 .. t, -1 below 0
     win = t[:, None] - (W - 1) + np.arange(W, dtype=np.int64)[None, :]
-    win[win < 0] = -1
+    win = np.where(win < 0, -1, cfg.base_row + win)
     idx[:, :W] = win
     kp = K - W
+    pool0 = cfg.base_row + cfg.ctx                     # kv row of pool row 0
     if kp > 0 and cfg.pool > 0:
         vis = np.minimum(cfg.pool, (t + 1) // cfg.ratio)  # visible pool rows per token
         full = vis <= kp
         # tokens whose visible pool fits: take all visible rows in order
         ar = np.arange(kp, dtype=np.int64)[None, :]
-        take = np.where(ar < vis[:, None], cfg.T + ar, -1)
+        take = np.where(ar < vis[:, None], pool0 + ar, -1)
         idx[full, W:] = take[full]
         # tokens with more visible rows than pool slots: seeded sample, sorted
         need = np.nonzero(~full)[0]
@@ -151,7 +194,7 @@ def make_indices(cfg: Config, rng: np.random.Generator) -> np.ndarray:
             keys[pcol >= vis[rows][:, None]] = np.inf
             pick = np.argpartition(keys, kp - 1, axis=1)[:, :kp]
             pick.sort(axis=1)
-            idx[rows, W:] = cfg.T + pick
+            idx[rows, W:] = pool0 + pick
     return idx.astype(dt)
 
 
@@ -164,7 +207,13 @@ def make_inputs(cfg: Config) -> dict:
     """
     rng = np.random.Generator(np.random.PCG64(cfg.seed))
     q = _normal_bf16(rng, (cfg.T, cfg.H, D))
-    kv = _normal_bf16(rng, (cfg.num_kv, D))
+    if cfg.base_row:
+        # rows of other sequences: a NaN pattern no slot names
+        kv = np.empty((cfg.num_kv, D), dtype=np.uint16)
+        kv[:cfg.base_row] = NAN_BITS
+        kv[cfg.base_row:] = _normal_bf16(rng, (cfg.num_kv - cfg.base_row, D))
+    else:
+        kv = _normal_bf16(rng, (cfg.num_kv, D))
     sink = rng.standard_normal(cfg.H, dtype=np.float32)
     idx = make_indices(cfg, rng)
     return {"q": q, "kv": kv, "idx": idx, "sink": sink if cfg.sink else None,

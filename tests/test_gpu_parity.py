@@ -97,14 +97,36 @@ def test_tiny_variants(B, variant, H):
     compare(out, lse, O, L)
 
 
+def _expected_trace(idx, num_kv, splits):
+    """Rows read per token, in gather order: within each of the call's slot
+    ranges (ceil(topk / splits) slots each), the valid slots' rows in slot
+    order, then -1 for the rest of the range (validity from the oracle)."""
+    T, K = idx.shape
+    valid = orc.valid_slots(idx, num_kv)
+    want = np.full((T, K), -1, dtype=np.int64)
+    chunk = -(-K // splits) if K else 0
+    for t in range(T):
+        for s in range(splits):
+            j0, j1 = min(K, s * chunk), min(K, (s + 1) * chunk)
+            rows = idx[t, j0:j1][valid[t, j0:j1]].astype(np.int64)
+            want[t, j0:j0 + len(rows)] = rows
+    return want
+
+
 @pytest.mark.parametrize("H", HEADS)
 @pytest.mark.parametrize("dtype", [np.int32, np.int64])
 @pytest.mark.parametrize("splits", [0, 1, 3])
 def test_read_trace_bit_exact(B, dtype, splits, H):
+    # The trace is written where each copy's source address is formed: the row
+    # every gather actually reads, recovered from that address.  It must list
+    # exactly the valid slots' rows (duplicates included, in slot order) and
+    # nothing else.
     cfg, x = _tiny_x(seed=5, H=H)
     x["idx"] = synth.inject_out_of_range(x["idx"].astype(dtype), cfg.num_kv, 9, frac=0.35)
+    x["idx"] = synth.inject_duplicates(x["idx"], cfg.num_kv, 10, frac=0.1)
     out, lse, tr = _run(B, x, splits=splits, trace=True)
-    want = np.where(orc.valid_slots(x["idx"], cfg.num_kv), x["idx"].astype(np.int64), -1)
+    used = B.sparse_mla_plan(cfg.T, cfg.H, cfg.topk, splits)[1]
+    want = _expected_trace(x["idx"], cfg.num_kv, used)
     np.testing.assert_array_equal(tr.cpu().numpy(), want)
 
 
@@ -344,7 +366,11 @@ def test_h128_large_logits(B, case, splits):
     # output alone is 2^-6: O is held to the bar plus one bf16 step of |O|
     # (output rounding and P's bf16 rounding); lse and the cosine to the bar.
     og = out.float().cpu().numpy().astype(np.float64)
-    assert np.all(np.abs(og - O) <= 2e-2 + 2.0 ** -8 * np.abs(O))
+    err = np.abs(og - O)
+    print(f"large logits {case} splits={splits}: max|dO|={err.max():.3e} "
+          f"max|O|={np.abs(O).max():.3f} max(|dO|/(2e-2+2^-8|O|))="
+          f"{(err / (2e-2 + 2.0 ** -8 * np.abs(O))).max():.3f}")
+    assert np.all(err <= 2e-2 + 2.0 ** -8 * np.abs(O))
     compare(out, lse, O, L, o_tol=np.inf)
 
 

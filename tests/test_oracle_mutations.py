@@ -64,6 +64,8 @@ def _mutant_token_forward(kind):
         if kind == "dedupe":
             rows = np.unique(rows)
         k = kv[rows]
+        if k.dtype == np.uint16:
+            k = orc.bf16_to_f64(k)
         sc = scale * scale if kind == "scale_squared" else scale
         s = sc * (q_t @ k.T)
         if kind == "neg_score":

@@ -22,11 +22,15 @@ EXPECTED_VALID = {
     "sweep_k640": 2088512,
     "h128": 1793728,
     "h128_long": 5994368,
+    "glm_k2048": 26171584,
+    "decode_h8_t1": 640,
+    "decode_h16_t16": 10240,
+    "decode_h128_t4": 2048,
 }
 
 
 def _closed_form_valid(cfg):
-    t = np.arange(cfg.T, dtype=np.int64)
+    t = cfg.pos0 + np.arange(cfg.T, dtype=np.int64)
     win = np.minimum(cfg.window, t + 1)
     vis = np.minimum(cfg.pool, (t + 1) // cfg.ratio)
     return int(win.sum() + np.minimum(vis, cfg.topk - cfg.window).sum())
@@ -38,7 +42,8 @@ def test_valid_count_closed_form(name):
     assert _closed_form_valid(cfg) == EXPECTED_VALID[name]
 
 
-@pytest.mark.parametrize("name", ["tiny", "sweep_k32", "sweep_k256", "h128"])
+@pytest.mark.parametrize("name", ["tiny", "sweep_k32", "sweep_k256", "h128", "glm_k2048",
+                                  "decode_h8_t1", "decode_h16_t16", "decode_h128_t4"])
 def test_index_structure(name):
     cfg = synth.CONFIGS[name]
     idx = synth.make_indices(cfg, np.random.Generator(np.random.PCG64(cfg.seed)))
@@ -46,20 +51,42 @@ def test_index_structure(name):
     assert idx.dtype == (np.int64 if cfg.index_dtype == "int64" else np.int32)
     W = cfg.window
     for t in range(0, cfg.T, max(1, cfg.T // 97)):
+        pos = cfg.pos0 + t                              # the token's position in its sequence
         row = idx[t].astype(np.int64)
-        exp_win = np.arange(t - W + 1, t + 1)
-        exp_win[exp_win < 0] = -1
+        exp_win = np.arange(pos - W + 1, pos + 1)
+        exp_win = np.where(exp_win < 0, -1, cfg.base_row + exp_win)
         np.testing.assert_array_equal(row[:W], exp_win)
         pool = row[W:]
         got = pool[pool >= 0]
-        vis = min(cfg.pool, (t + 1) // cfg.ratio)
+        vis = min(cfg.pool, (pos + 1) // cfg.ratio)
         assert len(got) == min(vis, cfg.topk - W)
         assert np.all(np.diff(got) > 0)                 # sorted, no repeats
-        p = got - cfg.T
-        assert np.all(p >= 0) and np.all(cfg.ratio * (p + 1) <= t + 1)
+        p = got - (cfg.base_row + cfg.ctx)
+        assert np.all(p >= 0) and np.all(cfg.ratio * (p + 1) <= pos + 1)
         assert np.all(pool[len(got):] == -1)
     valid = ((idx >= 0) & (idx < cfg.num_kv)).sum()
     assert valid == EXPECTED_VALID[name]
+    # rows of other sequences in a shared pool are never named
+    assert not np.any((idx >= 0) & (idx < cfg.base_row))
+
+
+def test_decode_configs_cover_the_sweep():
+    for h in synth.DECODE_H:
+        for t in synth.DECODE_T:
+            cfg = synth.CONFIGS[f"decode_h{h}_t{t}"]
+            assert (cfg.T, cfg.H, cfg.ctx) == (t, h, 8192)
+
+
+def test_shared_pool_rows_hold_nan():
+    # a small stand-in of the 2 GiB shared pool: the other sequences' rows are NaN
+    cfg = synth.CONFIGS["tiny"].with_(base_row=40)
+    x = synth.make_inputs(cfg)
+    assert x["kv"].shape == (cfg.num_kv, 512)
+    assert np.all(x["kv"][:40] == synth.NAN_BITS)
+    base = synth.make_inputs(synth.CONFIGS["tiny"])
+    np.testing.assert_array_equal(x["q"], base["q"])
+    np.testing.assert_array_equal(x["kv"][40:], base["kv"])
+    np.testing.assert_array_equal(np.where(x["idx"] >= 0, x["idx"] - 40, -1), base["idx"])
 
 
 def test_generator_is_deterministic():

@@ -1,18 +1,20 @@
 """The allocation-free entry point against the regular one (needs a GB300).
 
 ``sparse_mla_fwd_static_scratch`` serves callers that may not allocate device
-memory while they run (a stream under capture, a fixed memory budget, an
-allocator owned by another runtime): it runs the split-TOPK path with its
-partial results in the library's fixed scratch array.  Two calls in a row,
-with different shapes and inputs, must each agree with ``sparse_mla_fwd_ex``
-(the same split count: the same kernels, so bit for bit) and with the regular
-``sparse_mla_fwd`` within the parity tolerances.  The file is named to be
-collected last, so a run that stops at the first failure has already run
-every other test.
+memory while they run (work recorded into a stream capture, a fixed memory
+budget, an allocator owned by another runtime): it runs the split-TOPK path
+with its partial results in the library's fixed scratch array.  Two calls in a
+row, with different shapes and inputs, must each agree with
+``sparse_mla_fwd_ex`` (the same split count: the same kernels, so bit for
+bit), with the regular ``sparse_mla_fwd`` and with the fp64 oracle within the
+parity tolerances.  A repeated call must leave the device's free memory
+unchanged.  The file is named to be collected last, so a run that stops at the
+first failure has already run every other test.
 """
 import numpy as np
 import pytest
 
+from oracle import oracle as orc
 from sparse_mla_attention_token_gb300 import synth
 from tests.parity import compare, to_dev
 
@@ -54,6 +56,16 @@ def _one_call(B, x, num_splits, want_splits):
     assert torch.equal(o_s.view(torch.int16), o_x.view(torch.int16))
     assert torch.equal(l_s.view(torch.int32), l_x.view(torch.int32))
     compare(o_s, l_s, *_as_ref(o_r, l_r))
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(o_s, l_s, O, L)
+    # the same call again allocates nothing: the device's free memory is unchanged
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    B.sparse_mla_fwd_static_scratch(q, kv, idx, out, lse, sink, x["scale"],
+                                    num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.equal(out.view(torch.int16), o_x.view(torch.int16))
 
 
 def test_static_scratch_two_calls_in_a_row(B):
