@@ -66,14 +66,20 @@ def valid_slots(idx: np.ndarray, num_kv: int) -> np.ndarray:
 
 
 def token_forward(q_t: np.ndarray, kv: np.ndarray, idx_t: np.ndarray, num_kv: int,
-                  sink, scale: float):
-    """One token: returns (O [H, D] float64, lse [H] float64).
+                  sink, scale: float, d_v=None):
+    """One token: returns (O [H, d_v] float64, lse [H] float64).
 
     ``q_t`` is float64 ``[H, D]``, ``kv`` ``[num_kv, D]`` either float64 or
     bf16 bit patterns (uint16, widened exactly after the gather), ``sink`` a
-    float64 ``[H]`` array or None.
+    float64 ``[H]`` array or None.  Scores use all D columns; the values are
+    the first ``d_v`` columns of the same rows (default all D).  d_v < D is
+    the MLA layout with a positional part: each row is ``[no-pe | pe]`` and
+    only the no-pe part is a value ("Add DSv4 sparse MLA prefill Triton and
+    unified with MLA Gluon kernel on GFX950", the ``has_pe`` flag with a
+    64-wide positional part).
     """
     H, D = q_t.shape
+    dv = D if d_v is None else int(d_v)
     rows = np.asarray(idx_t).astype(np.int64)[valid_slots(idx_t, num_kv)]
     k = kv[rows]                                   # [v, D]; a duplicated row appears twice
     if k.dtype == np.uint16:
@@ -82,7 +88,7 @@ def token_forward(q_t: np.ndarray, kv: np.ndarray, idx_t: np.ndarray, num_kv: in
     m = s.max(axis=1) if rows.size else np.full(H, -np.inf)
     if sink is not None:
         m = np.maximum(m, sink)                    # sink folded into the max
-    out = np.zeros((H, D))
+    out = np.zeros((H, dv))
     lse = np.full(H, -np.inf)
     live = np.isfinite(m)                          # m = -inf: nothing valid and no finite sink
     if np.any(live):
@@ -91,28 +97,31 @@ def token_forward(q_t: np.ndarray, kv: np.ndarray, idx_t: np.ndarray, num_kv: in
         den = e.sum(axis=1)
         if sink is not None:
             den = den + np.exp(sink[live] - ml)    # sink in the denominator only
-        out[live] = (e @ k) / den[:, None]
+        out[live] = (e @ k[:, :dv]) / den[:, None]
         lse[live] = ml + np.log(den)
     return out, lse
 
 
 def sparse_mla_fwd(q_bits: np.ndarray, kv_bits: np.ndarray, idx: np.ndarray, sink,
-                   scale: float, tokens=None):
+                   scale: float, tokens=None, d_v=None):
     """The whole op (or a subset of tokens) in float64.
 
     q_bits: uint16 bf16 bits ``[T, H, D]``; kv_bits: uint16 bf16 bits
     ``[num_kv, D]``; idx: int32/int64 ``[T, TOPK]``; sink: float32 ``[H]`` or
-    None; tokens: optional iterable of token ids (default all).
-    Returns (O float64 ``[n, H, D]``, lse float64 ``[n, H]``) for those tokens.
+    None; tokens: optional iterable of token ids (default all); d_v: value
+    width (the first d_v columns of each kv row; default D).
+    Returns (O float64 ``[n, H, d_v]``, lse float64 ``[n, H]``) for those tokens.
     """
     num_kv = kv_bits.shape[0]
     kv = np.asarray(kv_bits, dtype=np.uint16)      # rows are widened once gathered
     sk = None if sink is None else np.asarray(sink, dtype=np.float32).astype(np.float64)
     T, H, D = q_bits.shape
+    dv = D if d_v is None else int(d_v)
     toks = range(T) if tokens is None else list(tokens)
     n = len(toks)
-    O = np.zeros((n, H, D))
+    O = np.zeros((n, H, dv))
     L = np.full((n, H), -np.inf)
     for i, t in enumerate(toks):
-        O[i], L[i] = token_forward(bf16_to_f64(q_bits[t]), kv, idx[t], num_kv, sk, scale)
+        O[i], L[i] = token_forward(bf16_to_f64(q_bits[t]), kv, idx[t], num_kv, sk, scale,
+                                   d_v=dv)
     return O, L
