@@ -21,7 +21,10 @@ other workload (the small-head workload, the H=8 top-k sweep with the sink on
 and off, the long H=128 workload, the GLM-shaped top-k 2048 call, the tiny
 workload and decode-sized calls of 1-16 tokens), each timed the same way (L2
 flushed before every timed call, CUDA events on the launching stream), with
-its roofline fractions and the fp64 oracle timed on a bounded token sample.
+its roofline fractions and the fp64 oracle timed on a bounded token sample;
+``fp8_small_head`` / ``fp8_sweep_k640``: the same workloads on an fp8 KV
+cache; and ``bwd_h128``: the training backward on the T=4096 H=128 topk=512
+workload.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this op
 has) on bounded token samples of the same workload, on rank 0 only.
@@ -307,6 +310,131 @@ def measure_workload(name: str, args, dev, flush, stream, peaks: dict) -> dict:
     return e
 
 
+def measure_fp8(name: str, args, dev, flush, stream, peaks: dict) -> dict:
+    """The forward on an fp8 KV cache of the workload's kv (e4m3 codes + one fp32
+    scale per 128 columns): device time per call and the roofline with 528
+    gathered bytes per valid slot (512 codes + 16 scale bytes)."""
+    import torch
+    from sparse_mla_attention_token_gb300 import binding as B
+    cfg = synth.CONFIGS[name]
+    x = synth.make_inputs(cfg)
+    kv8, sc = synth.fp8_cache(x["kv"])
+    counts = roofline.count(x["idx"], cfg.num_kv, cfg.H, cfg.sink)
+    q = torch.from_numpy(x["q"].view(np.int16)).view(torch.bfloat16).to(dev)
+    k8 = torch.from_numpy(kv8).to(dev)
+    s8 = torch.from_numpy(sc).to(dev)
+    idx = torch.from_numpy(x["idx"]).to(dev)
+    sink = torch.from_numpy(x["sink"]).to(dev) if x["sink"] is not None else None
+    out = torch.empty_like(q)
+    lse = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device=dev)
+
+    def step():
+        B.sparse_mla_fwd_fp8kv(q, k8, s8, idx, sink, x["scale"], out=out, lse=lse)
+
+    ms = time_calls(step, args.pw_steps, 3, flush, stream)
+    if B.sparse_mla_device_status() != 0:
+        raise RuntimeError(f"device status not OK after fp8 {name}")
+    med = statistics.median(ms)
+    fixed = counts.fixed_bytes
+    gathered = fixed + 528.0 * counts.valid
+    t_flop = counts.flops / (peaks["bf16_tflops"] * 1e12)
+    t_mem = gathered / (peaks["hbm_gbs"] * 1e9)
+    family, splits, launches = B.sparse_mla_plan(cfg.T, cfg.H, cfg.topk)
+    e = {"workload": workload_desc(cfg) + " (fp8 e4m3 cache, one fp32 scale per 128 columns)",
+         "kernel": "smallh_fwd_kernel (fp8 cache)", "ms_per_call": med, "ms_min": min(ms),
+         "ms_max": max(ms), "steps": len(ms), "tflops": counts.flops / (med * 1e-3) / 1e12,
+         "bound": "tensor" if t_flop >= t_mem else "hbm",
+         "frac_of_roofline_gathered": max(t_flop, t_mem) / (med * 1e-3),
+         "roofline_gathered_ms": max(t_flop, t_mem) * 1e3,
+         "bytes_counted": "Q+O+lse+indices+sink + 528 B (codes + scales) per valid slot",
+         "splits": splits, "gpu_launches": len(ms) * launches}
+    if args.cpu_seconds > 0:
+        from oracle import fp8kv
+        import time as _time
+        n = 4
+        t0 = _time.perf_counter()
+        fp8kv.sparse_mla_fwd_fp8kv(x["q"], kv8, sc, x["idx"], x["sink"], x["scale"],
+                                   tokens=range(cfg.T - n, cfg.T))
+        per = (_time.perf_counter() - t0) / n
+        n = int(max(4, min(cfg.T, min(args.cpu_seconds, 2.0) / max(per, 1e-6))))
+        toks = list(range(cfg.T - n, cfg.T))
+        t0 = _time.perf_counter()
+        fp8kv.sparse_mla_fwd_fp8kv(x["q"], kv8, sc, x["idx"], x["sink"], x["scale"], tokens=toks)
+        el = _time.perf_counter() - t0
+        valid = ((x["idx"][toks] >= 0) & (x["idx"][toks] < cfg.num_kv)).sum()
+        e["cpu_baseline"] = {"value": 4.0 * cfg.H * 512 * float(valid) / el / 1e12,
+                             "unit": "TFLOP/s", "cores": _blas_threads(), "kind": "oracle",
+                             "sample": f"tokens {toks[0]}..{toks[-1]} ({n} tokens, {el:.2f} s, "
+                                       f"fp64 numpy fp8-cache oracle)"}
+    del q, k8, s8, idx, sink, out, lse
+    return e
+
+
+def measure_backward(name: str, args, dev, flush, stream, peaks: dict) -> dict:
+    """The training backward on one workload: the forward's O / lse (CUDA) and a
+    seeded dO feed ``sparse_mla_bwd``; device time per call, roofline, oracle."""
+    import torch
+    from sparse_mla_attention_token_gb300 import binding as B
+    cfg = synth.CONFIGS[name]
+    x = synth.make_inputs(cfg)
+    counts = roofline.count(x["idx"], cfg.num_kv, cfg.H, cfg.sink)
+    q, kv, idx, sink, keep = _device_inputs(x, cfg, dev)
+    out, lse = B.sparse_mla_fwd(q, kv, idx, sink, x["scale"])
+    dbits = synth.make_dout(cfg)
+    dout = torch.from_numpy(dbits.view(np.int16)).view(torch.bfloat16).to(dev)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dkv = torch.empty(kv.shape, dtype=torch.float32, device=dev)
+    dsink = torch.empty(cfg.H, dtype=torch.float32, device=dev) if sink is not None else None
+    ws = torch.empty(B.sparse_mla_bwd_workspace(cfg.T, cfg.H, cfg.topk, cfg.num_kv),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        B.sparse_mla_bwd(q, kv, idx, out, lse, dout, sink, x["scale"], dq=dq, dkv=dkv,
+                         dsink=dsink, workspace=ws)
+
+    ms = time_calls(step, args.pw_steps, 3, flush, stream)
+    torch.cuda.synchronize()
+    med = statistics.median(ms)
+    flops = 10.0 * cfg.H * 512 * counts.valid            # S, dP, dq and the two dkv terms
+    flops_all = 10.0 * cfg.T * cfg.H * cfg.topk * 512     # the page's all-slot count
+    TH = cfg.T * cfg.H
+    # algorithmic bytes: q, O, dO in (bf16), lse, indices, one gathered kv row per
+    # valid slot, dq out (fp32), dkv out (fp32, every row)
+    nbytes = (3.0 * TH * 1024 + 4.0 * TH + cfg.T * cfg.topk * x["idx"].dtype.itemsize +
+              counts.valid * 1024.0 + TH * 2048.0 + cfg.num_kv * 2048.0)
+    t_flop = flops / (peaks["bf16_tflops"] * 1e12)
+    t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
+    e = {"workload": workload_desc(cfg) + " (backward: dq, dkv, dsink)",
+         "kernels": "bwd_delta, bwd_dq (mma.sync), bwd_interm (mma.sync), inverted index "
+                    "(count, scan, fill), bwd_gather, bwd_dsink",
+         "ms_per_call": med, "ms_min": min(ms), "ms_max": max(ms), "steps": len(ms),
+         "tflops": flops / (med * 1e-3) / 1e12,
+         "tflops_all_slots": flops_all / (med * 1e-3) / 1e12,
+         "bound": "tensor" if t_flop >= t_mem else "hbm",
+         "frac_of_roofline": max(t_flop, t_mem) / (med * 1e-3),
+         "tensor_frac": t_flop / (med * 1e-3), "roofline_ms": max(t_flop, t_mem) * 1e3,
+         "workspace_bytes": int(ws.numel())}
+    if args.cpu_seconds > 0:
+        from oracle import backward as obwd
+        import time as _time
+        toks = list(range(cfg.T - 4, cfg.T))    # calibrate on full-length lists
+        t0 = _time.perf_counter()
+        obwd.sparse_mla_bwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"], dbits, tokens=toks)
+        per = (_time.perf_counter() - t0) / len(toks)
+        n = int(max(4, min(cfg.T, min(args.cpu_seconds, 2.0) / max(per, 1e-6))))
+        toks = list(range(cfg.T - n, cfg.T))     # the last tokens: full-length lists
+        t0 = _time.perf_counter()
+        obwd.sparse_mla_bwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"], dbits, tokens=toks)
+        el = _time.perf_counter() - t0
+        valid = ((x["idx"][toks] >= 0) & (x["idx"][toks] < cfg.num_kv)).sum()
+        e["cpu_baseline"] = {"value": 10.0 * cfg.H * 512 * float(valid) / el / 1e12,
+                             "unit": "TFLOP/s", "cores": _blas_threads(), "kind": "oracle",
+                             "sample": f"tokens {toks[0]}..{toks[-1]} ({n} tokens, {el:.2f} s, "
+                                       f"fp64 numpy backward oracle)"}
+    del q, kv, idx, sink, keep, out, lse, dout, dq, dkv, dsink, ws
+    return e
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, cfg) -> None:
     import torch
@@ -454,6 +582,12 @@ def run_ours(args, cfg) -> None:
             if n == cfg.name:
                 continue
             pw[n] = measure_workload(n, args, dev, flush, stream, peaks)
+            torch.cuda.empty_cache()
+        if args.per_workload == "all":
+            for n in ("small_head", "sweep_k640"):
+                pw[f"fp8_{n}"] = measure_fp8(n, args, dev, flush, stream, peaks)
+                torch.cuda.empty_cache()
+            pw["bwd_h128"] = measure_backward("h128", args, dev, flush, stream, peaks)
             torch.cuda.empty_cache()
         pw_sampler.mark(p0, time.time())
         line["per_workload"] = pw

@@ -122,6 +122,55 @@ smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_
                                 int64_t* read_trace);
 
 /*
+ * sparse_mla_fwd_dims -- the op at other head dims, and with a positional part.
+ *
+ *   d_qk         score width: q is [T, H, d_qk], kv is [num_kv, d_qk] (bf16).
+ *   d_v          value width: the values are the first d_v columns of each kv
+ *                row; out is [T, H, d_v] bf16.
+ *   Supported (d_qk, d_v): (512, 512) -- exactly sparse_mla_fwd; (128, 128)
+ *   and (576, 576), K == V at the head dims "Tuned sparse MLA prefill for
+ *   DSv4.1-Flash TP4" tests; (576, 512), the MLA layout of "Add DSv4 sparse
+ *   MLA prefill Triton and unified with MLA Gluon kernel on GFX950" with
+ *   has_pe = True: each row is [512 no-pe | 64 pe] (q the same), the scores
+ *   use all 576 columns and only the no-pe part is a value.  Other pairs
+ *   return SMLA_ERR_BAD_SHAPE.  scale is the caller's (1/sqrt(d_qk) is the
+ *   usual choice).  Other arguments, layouts, errors and the allocation of
+ *   the split path's workspace: as sparse_mla_fwd.  Pairs other than
+ *   (512, 512) run on the small-head kernel family for every H.
+ */
+smla_status_t sparse_mla_fwd_dims(const void* q, const void* kv, const void* topk_indices,
+                                  int32_t index_dtype, const float* attn_sink, float scale,
+                                  void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
+                                  int32_t topk, int32_t d_qk, int32_t d_v, void* stream);
+
+/*
+ * sparse_mla_fwd_fp8kv -- the op on an fp8 KV cache.
+ *
+ * The pages leave the fp8 cache out ("Add DSv4 sparse MLA prefill Triton and
+ * unified with MLA Gluon kernel on GFX950": the fp8 paged decode cache is not
+ * part of that change) and make the bf16 entry reject an fp8 pool with a dtype
+ * error ("Tuned sparse MLA prefill for DSv4.1-Flash TP4", which the Python
+ * binding's sparse_mla_fwd follows).  This entry point serves such a cache in
+ * the layout this library reads it in:
+ *
+ *   kv_fp8       [num_kv, 512] bytes, OCP FP8 E4M3 (e4m3fn) codes, 16-byte
+ *                aligned.
+ *   kv_scale     [num_kv, 4] fp32, 16-byte aligned: one scale per 128-column
+ *                block; the row's value in column c is
+ *                decode(kv_fp8[r, c]) * kv_scale[r, c / 128].
+ *   Everything else as sparse_mla_fwd: q, out bf16 [T, H, 512], the same
+ *   checks, the split path's stream-ordered workspace.  Every H runs on the
+ *   small-head kernel family.  Only the rows valid slots name are read.
+ * Numerics: the codes are decoded exactly into bf16; the scales are applied in
+ * fp32 to the partial scores and, per block, to P before its bf16 rounding.
+ */
+smla_status_t sparse_mla_fwd_fp8kv(const void* q, const void* kv_fp8, const float* kv_scale,
+                                   const void* topk_indices, int32_t index_dtype,
+                                   const float* attn_sink, float scale, void* out, float* lse,
+                                   int64_t T, int32_t H, int64_t num_kv, int32_t topk,
+                                   void* stream);
+
+/*
  * sparse_mla_fwd_static_scratch -- the split-TOPK path without any allocation.
  *
  * The pages have no counterpart to this entry point.  It exists for callers
@@ -202,6 +251,57 @@ smla_status_t sparse_mla_fwd_host(const void* q_host, const void* kv_host,
 smla_status_t sparse_mla_fwd_host_workspace(int64_t T, int32_t H, int32_t topk, int64_t num_kv,
                                             int32_t index_dtype, int32_t has_sink,
                                             uint64_t* bytes);
+
+/*
+ * sparse_mla_bwd -- the training backward ("Sparse MLA training backward",
+ * aiter PR #4766, sections "Contract" and "Structure").
+ *
+ * For the forward above, with its output O and sink-inclusive lse saved, and
+ * the output gradient dO, over the valid slots of each token and head:
+ *   P_j = exp(scale <q, kv[r_j]> - lse)        (lse from the forward)
+ *   delta = <O, dO>,  dS_j = P_j (<dO, kv[r_j]> - delta)
+ *   dq         = scale sum_j dS_j kv[r_j]
+ *   dkv[r_j]  += scale dS_j q + P_j dO          (K == V: both terms on the row;
+ *                                               summed over heads and slots)
+ *   dsink[h]   = -sum_t exp(sink[h] - lse[t,h]) delta[t,h]
+ *
+ *   q, kv, topk_indices, index_dtype, attn_sink, scale, T, H, num_kv: as
+ *                sparse_mla_fwd (same layouts and checks).
+ *   out          [T, H, 512] bf16: the forward's output O.
+ *   lse          [T, H] fp32: the forward's lse (sink-inclusive).
+ *   dout         [T, H, 512] bf16: dO, 16-byte aligned.
+ *   dq           [T, H, 512] fp32, 16-byte aligned (written whole).
+ *   dkv          [num_kv, 512] fp32, 16-byte aligned (written whole: rows no
+ *                valid slot names get 0).
+ *   dsink        [H] fp32 or NULL (not computed); 0 when attn_sink is NULL.
+ *   topk         0..2048; T * topk < 2^31.
+ *   workspace    DEVICE memory of at least sparse_mla_bwd_workspace() bytes,
+ *                256-byte aligned, owned by the caller and not touched by
+ *                other work until `stream` has passed the call; the call
+ *                allocates nothing.
+ *   Errors       as sparse_mla_fwd, plus SMLA_ERR_WORKSPACE; all before any
+ *                CUDA call.  Outputs and the workspace may not overlap inputs
+ *                or each other.
+ * Numerics: the contractions run in bf16 with fp32 accumulation; P and
+ * scale * dS are rounded to bf16 before the two contractions over them (the
+ * dq and the per-slot dkv terms).  The summation order of a kv row's terms
+ * follows an atomic fill, so dkv can differ between calls in its last bits.
+ */
+smla_status_t sparse_mla_bwd(const void* q, const void* kv, const void* topk_indices,
+                             int32_t index_dtype, const float* attn_sink, float scale,
+                             const void* out, const float* lse, const void* dout, float* dq,
+                             float* dkv, float* dsink, int64_t T, int32_t H, int64_t num_kv,
+                             int32_t topk, void* workspace, uint64_t workspace_bytes,
+                             void* stream);
+
+/*
+ * sparse_mla_bwd_workspace -- device workspace bytes sparse_mla_bwd needs for
+ * these sizes (host only, no CUDA call): per-row delta, P and scale * dS per
+ * valid slot and head (bf16), the compacted rows, each slot's dkv term
+ * (fp32, T * topk * 2 KB) and the inverted index.
+ */
+smla_status_t sparse_mla_bwd_workspace(int64_t T, int32_t H, int32_t topk, int64_t num_kv,
+                                       uint64_t* bytes);
 
 /*
  * sparse_mla_plan -- what sparse_mla_fwd_ex would launch, without launching.

@@ -41,6 +41,12 @@ SIGNATURES = {
     "sparse_mla_fwd_static_scratch": (_I32, _FWD_ARGS + [_I32]),
     "sparse_mla_fwd_host": (_I32, _FWD_ARGS[:-1] + [_P, _U64, _P]),
     "sparse_mla_fwd_host_workspace": (_I32, [_I64, _I32, _I32, _I64, _I32, _I32, _P]),
+    "sparse_mla_fwd_dims": (_I32, _FWD_ARGS[:-1] + [_I32, _I32, _P]),
+    "sparse_mla_fwd_fp8kv": (_I32, [_P, _P, _P, _P, _I32, _P, _F32, _P, _P, _I64, _I32, _I64,
+                                    _I32, _P]),
+    "sparse_mla_bwd": (_I32, [_P, _P, _P, _I32, _P, _F32, _P, _P, _P, _P, _P, _P, _I64, _I32,
+                              _I64, _I32, _P, _U64, _P]),
+    "sparse_mla_bwd_workspace": (_I32, [_I64, _I32, _I32, _I64, _P]),
     "sparse_mla_plan": (_I32, [_I64, _I32, _I32, _I32, _P, _P, _P]),
     "sparse_mla_launch_config": (_I32, [_I64, _I32, _I32, _I64, _I32, _P, _P, _P, _P]),
     "sparse_mla_device_status": (_I32, [_P]),
@@ -312,4 +318,176 @@ def sparse_mla_fwd_host(q, kv, topk_indices, out, lse, attn_sink=None, workspace
             _stream_ptr(stream))
     if st != SMLA_OK:
         raise SparseMLAError(st, "sparse_mla_fwd_host")
+    return out, lse
+
+
+def sparse_mla_bwd_workspace(T: int, H: int, topk: int, num_kv: int) -> int:
+    """Device workspace bytes of :func:`sparse_mla_bwd` for these sizes."""
+    n = ctypes.c_uint64(0)
+    st = lib().sparse_mla_bwd_workspace(int(T), int(H), int(topk), int(num_kv), ctypes.byref(n))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_bwd_workspace")
+    return int(n.value)
+
+
+def sparse_mla_bwd(q, kv, topk_indices, out, lse, dout, attn_sink=None,
+                   scale: Optional[float] = None, dq=None, dkv=None, dsink=None, workspace=None,
+                   stream=None):
+    """Training backward; returns ``(dq, dkv, dsink)`` (fp32; dsink None without a sink).
+
+    ``out`` and ``lse`` are the forward's outputs for the same inputs, ``dout``
+    the output gradient (bf16, q's shape).  ``dq`` / ``dkv`` / ``dsink`` and the
+    CUDA uint8 ``workspace`` (at least :func:`sparse_mla_bwd_workspace` bytes)
+    are allocated when not given.
+    """
+    import torch
+    if q.dtype != torch.bfloat16 or kv.dtype != q.dtype:
+        raise RuntimeError(f"q and kv must be bfloat16, got {q.dtype} / {kv.dtype}")
+    if out.dtype != torch.bfloat16 or dout.dtype != torch.bfloat16:
+        raise RuntimeError("out and dout must be bfloat16")
+    if out.shape != q.shape or dout.shape != q.shape:
+        raise RuntimeError("out and dout must have q's shape")
+    if topk_indices.dtype not in (torch.int32, torch.int64):
+        raise RuntimeError(f"topk_indices must be int32 or int64, got {topk_indices.dtype}")
+    T, H, _ = q.shape
+    dev = q.device
+    if tuple(lse.shape) != (T, H) or lse.dtype != torch.float32:
+        raise RuntimeError(f"lse must be float32 [{T}, {H}]")
+    for n, x in (("q", q), ("kv", kv), ("topk_indices", topk_indices), ("out", out),
+                 ("lse", lse), ("dout", dout)):
+        _check_dev(n, x, dev)
+        if not x.is_contiguous():
+            raise RuntimeError(f"{n} must be contiguous")
+    if attn_sink is not None:
+        _check_dev("attn_sink", attn_sink, dev)
+        if attn_sink.dtype != torch.float32 or tuple(attn_sink.shape) != (H,):
+            raise RuntimeError(f"attn_sink must be float32 [{H}]")
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    if dkv is None:
+        dkv = torch.empty(kv.shape, dtype=torch.float32, device=dev)
+    if dsink is None and attn_sink is not None:
+        dsink = torch.empty(H, dtype=torch.float32, device=dev)
+    for n, x, shp in (("dq", dq, tuple(q.shape)), ("dkv", dkv, tuple(kv.shape))):
+        _check_dev(n, x, dev)
+        if x.dtype != torch.float32 or tuple(x.shape) != shp or not x.is_contiguous():
+            raise RuntimeError(f"{n} must be contiguous float32 {shp}")
+    topk = topk_indices.shape[1]
+    need = sparse_mla_bwd_workspace(T, H, topk, kv.shape[0])
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check_dev("workspace", workspace, dev)
+    if scale is None:
+        scale = 512 ** -0.5
+    idt = SMLA_IDX_INT64 if topk_indices.dtype == torch.int64 else SMLA_IDX_INT32
+    with torch.cuda.device(dev):
+        st = lib().sparse_mla_bwd(
+            q.data_ptr(), kv.data_ptr() if kv.numel() else None,
+            topk_indices.data_ptr() if topk_indices.numel() else None, idt,
+            attn_sink.data_ptr() if attn_sink is not None else None, float(scale),
+            out.data_ptr(), lse.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+            dkv.data_ptr() if dkv.numel() else None,
+            dsink.data_ptr() if dsink is not None else None, T, H, kv.shape[0], topk,
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_ptr(stream))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_bwd")
+    return dq, dkv, dsink
+
+
+def sparse_mla_fwd_dims(q, kv, topk_indices, attn_sink=None, scale: Optional[float] = None,
+                        d_v: Optional[int] = None, out=None, lse=None, stream=None):
+    """The forward at head dim ``d_qk = q.shape[-1]`` with values the first ``d_v``
+    columns of each kv row (default all); returns ``(out [T, H, d_v], lse)``.
+
+    Supported (d_qk, d_v): (512, 512), (128, 128), (576, 576) and (576, 512)
+    (rows ``[512 no-pe | 64 pe]``: the positional part enters the scores only).
+    ``scale`` defaults to 1/sqrt(d_qk).
+    """
+    import torch
+    if q.dim() != 3 or kv.dim() != 2 or kv.shape[-1] != q.shape[-1]:
+        raise RuntimeError(f"q [T, H, D] and kv [num_kv, D] must share D, got "
+                           f"{tuple(q.shape)} / {tuple(kv.shape)}")
+    if q.dtype != torch.bfloat16 or kv.dtype != q.dtype:
+        raise RuntimeError(f"kv dtype mismatch or not bfloat16: q {q.dtype}, kv {kv.dtype}")
+    if topk_indices.dtype not in (torch.int32, torch.int64):
+        raise RuntimeError(f"topk_indices must be int32 or int64, got {topk_indices.dtype}")
+    T, H, d_qk = q.shape
+    dv = d_qk if d_v is None else int(d_v)
+    dev = q.device
+    for n, x in (("q", q), ("kv", kv), ("topk_indices", topk_indices)):
+        _check_dev(n, x, dev)
+        if not x.is_contiguous():
+            raise RuntimeError(f"{n} must be contiguous")
+    if attn_sink is not None:
+        _check_dev("attn_sink", attn_sink, dev)
+        if attn_sink.dtype != torch.float32 or tuple(attn_sink.shape) != (H,):
+            raise RuntimeError(f"attn_sink must be float32 [{H}]")
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if tuple(out.shape) != (T, H, dv) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise RuntimeError(f"out must be contiguous bfloat16 [{T}, {H}, {dv}]")
+    if scale is None:
+        scale = d_qk ** -0.5
+    idt = SMLA_IDX_INT64 if topk_indices.dtype == torch.int64 else SMLA_IDX_INT32
+    with torch.cuda.device(dev):
+        st = lib().sparse_mla_fwd_dims(
+            q.data_ptr(), kv.data_ptr() if kv.numel() else None,
+            topk_indices.data_ptr() if topk_indices.numel() else None, idt,
+            attn_sink.data_ptr() if attn_sink is not None else None, float(scale),
+            out.data_ptr(), lse.data_ptr(), T, H, kv.shape[0], topk_indices.shape[1],
+            d_qk, dv, _stream_ptr(stream))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_fwd_dims")
+    return out, lse
+
+
+def sparse_mla_fwd_fp8kv(q, kv_fp8, kv_scale, topk_indices, attn_sink=None,
+                         scale: Optional[float] = None, out=None, lse=None, stream=None):
+    """The forward on an fp8 KV cache; returns ``(out, lse)``.
+
+    ``kv_fp8`` is ``[num_kv, 512]`` uint8 (or torch.float8_e4m3fn) e4m3 codes and
+    ``kv_scale`` ``[num_kv, 4]`` float32, one scale per 128-column block.
+    """
+    import torch
+    if q.dim() != 3 or q.shape[-1] != 512 or q.dtype != torch.bfloat16:
+        raise RuntimeError(f"q must be bfloat16 [T, H, 512], got {q.dtype} {tuple(q.shape)}")
+    if kv_fp8.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise RuntimeError(f"kv_fp8 must hold e4m3 codes (uint8 / float8_e4m3fn), got {kv_fp8.dtype}")
+    if kv_fp8.dim() != 2 or kv_fp8.shape[-1] != 512:
+        raise RuntimeError(f"kv_fp8 must be [num_kv, 512], got {tuple(kv_fp8.shape)}")
+    if kv_scale.dtype != torch.float32 or tuple(kv_scale.shape) != (kv_fp8.shape[0], 4):
+        raise RuntimeError(f"kv_scale must be float32 [{kv_fp8.shape[0]}, 4]")
+    if topk_indices.dtype not in (torch.int32, torch.int64):
+        raise RuntimeError(f"topk_indices must be int32 or int64, got {topk_indices.dtype}")
+    T, H, _ = q.shape
+    dev = q.device
+    for n, x in (("q", q), ("kv_fp8", kv_fp8), ("kv_scale", kv_scale),
+                 ("topk_indices", topk_indices)):
+        _check_dev(n, x, dev)
+        if not x.is_contiguous():
+            raise RuntimeError(f"{n} must be contiguous")
+    if attn_sink is not None:
+        _check_dev("attn_sink", attn_sink, dev)
+        if attn_sink.dtype != torch.float32 or tuple(attn_sink.shape) != (H,):
+            raise RuntimeError(f"attn_sink must be float32 [{H}]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if scale is None:
+        scale = 512 ** -0.5
+    idt = SMLA_IDX_INT64 if topk_indices.dtype == torch.int64 else SMLA_IDX_INT32
+    with torch.cuda.device(dev):
+        st = lib().sparse_mla_fwd_fp8kv(
+            q.data_ptr(), kv_fp8.data_ptr() if kv_fp8.numel() else None,
+            kv_scale.data_ptr() if kv_scale.numel() else None,
+            topk_indices.data_ptr() if topk_indices.numel() else None, idt,
+            attn_sink.data_ptr() if attn_sink is not None else None, float(scale),
+            out.data_ptr(), lse.data_ptr(), T, H, kv_fp8.shape[0], topk_indices.shape[1],
+            _stream_ptr(stream))
+    if st != SMLA_OK:
+        raise SparseMLAError(st, "sparse_mla_fwd_fp8kv")
     return out, lse

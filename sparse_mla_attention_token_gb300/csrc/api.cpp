@@ -70,19 +70,27 @@ int device_sms() {
   return per_dev[dev];
 }
 
+// kernel family and split count; `dims512` false for other head dims (the
+// tcgen05 kernel is built for 512-wide rows only)
 smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int64_t num_kv, int32_t num_splits,
-                        int num_sms, Plan* pl) {
+                        int num_sms, Plan* pl, bool dims512 = true) {
   if (num_splits < 0 || num_splits > kMaxSplits) return SMLA_ERR_BAD_SPLITS;
   const int min_splits =
       std::max(1, (topk + smla::kSmallHMaxSlots - 1) / smla::kSmallHMaxSlots);
   int splits;
+  const int64_t ctas = T * ((H + 15) / 16);          // small-head CTAs without splits
+  const int decode_splits = (topk + 127) / 128;      // about 128 slots per split
   if (num_splits > 0) {
     splits = num_splits;
-  } else if (smla::h128_supported(T, H, topk, num_kv)) {
+  } else if (decode_splits >= 2 && ctas > 0 && ctas * decode_splits <= 2 * num_sms) {
+    // a decode-sized call (a few tokens): the split path with ~128 slots per
+    // split, while its grid fits the GPU twice (measured faster than the
+    // persistent kernels and than more, shorter splits for 1-16 tokens)
+    splits = std::min(decode_splits, 16);
+  } else if (dims512 && smla::h128_supported(T, H, topk, num_kv)) {
     splits = 1;
   } else {
     // enough CTAs to cover the GPU twice; each split keeps >= 64 slots
-    const int64_t ctas = T * ((H + 15) / 16);
     splits = 1;
     if (ctas > 0 && ctas < 2 * num_sms) {
       const int64_t want = (2 * num_sms + ctas - 1) / ctas;
@@ -93,7 +101,7 @@ smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int64_t num_kv, int3
   splits = std::max(splits, min_splits);
   if (num_splits > 0 && splits != num_splits) return SMLA_ERR_BAD_SPLITS;  // too few for topk
   if (splits > kMaxSplits) return SMLA_ERR_BAD_SPLITS;
-  const bool tc = (splits == 1) && smla::h128_supported(T, H, topk, num_kv);
+  const bool tc = dims512 && (splits == 1) && smla::h128_supported(T, H, topk, num_kv);
   pl->family = tc ? 1 : 0;
   pl->splits = splits;
   pl->launches = (T == 0) ? 0 : (splits > 1 ? 2 : 1);
@@ -102,7 +110,9 @@ smla_status_t make_plan(int64_t T, int32_t H, int32_t topk, int64_t num_kv, int3
 
 smla_status_t validate(const void* q, const void* kv, const void* idx, int32_t index_dtype,
                        const float* sink, float scale, void* out, float* lse, int64_t T,
-                       int32_t H, int64_t num_kv, int32_t topk, const int64_t* trace) {
+                       int32_t H, int64_t num_kv, int32_t topk, const int64_t* trace,
+                       int32_t d_qk = smla::kHeadDim, int32_t d_v = smla::kHeadDim,
+                       uint64_t kv_row_bytes = 0) {
   if (T < 0 || num_kv < 0 || num_kv >= (int64_t(1) << 31) || topk < 0) return SMLA_ERR_BAD_SHAPE;
   if (T > (int64_t(1) << 31) - 1) return SMLA_ERR_BAD_SHAPE;
   if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
@@ -117,8 +127,9 @@ smla_status_t validate(const void* q, const void* kv, const void* idx, int32_t i
   if (!aligned(q, 16) || !aligned(out, 16) || (kv && !aligned(kv, 16)) || !aligned(lse, 4) ||
       (idx && !aligned(idx, isz)) || (sink && !aligned(sink, 4)) || (trace && !aligned(trace, 8)))
     return SMLA_ERR_MISALIGNED;
-  const uint64_t qb = uint64_t(T) * H * smla::kHeadDim * 2;
-  const uint64_t kvb = uint64_t(num_kv) * smla::kHeadDim * 2;
+  const uint64_t qb = uint64_t(T) * H * d_qk * 2;
+  const uint64_t ob = uint64_t(T) * H * d_v * 2;
+  const uint64_t kvb = uint64_t(num_kv) * (kv_row_bytes ? kv_row_bytes : uint64_t(d_qk) * 2);
   const uint64_t ib = uint64_t(T) * topk * isz;
   const uint64_t lb = uint64_t(T) * H * 4;
   const uint64_t sb = sink ? uint64_t(H) * 4 : 0;
@@ -126,11 +137,11 @@ smla_status_t validate(const void* q, const void* kv, const void* idx, int32_t i
   const void* ins[4] = {q, kv, idx, sink};
   const uint64_t inb[4] = {qb, kvb, ib, sb};
   for (int i = 0; i < 4; ++i) {
-    if (overlap(out, qb, ins[i], inb[i]) || overlap(lse, lb, ins[i], inb[i]) ||
+    if (overlap(out, ob, ins[i], inb[i]) || overlap(lse, lb, ins[i], inb[i]) ||
         overlap(trace, tb, ins[i], inb[i]))
       return SMLA_ERR_ALIASING;
   }
-  if (overlap(out, qb, lse, lb) || overlap(out, qb, trace, tb) || overlap(lse, lb, trace, tb))
+  if (overlap(out, ob, lse, lb) || overlap(out, ob, trace, tb) || overlap(lse, lb, trace, tb))
     return SMLA_ERR_ALIASING;
   return SMLA_OK;
 }
@@ -138,12 +149,16 @@ smla_status_t validate(const void* q, const void* kv, const void* idx, int32_t i
 smla_status_t run(const void* q, const void* kv, const void* idx, int32_t index_dtype,
                   const float* sink, float scale, void* out, float* lse, int64_t T, int32_t H,
                   int64_t num_kv, int32_t topk, void* stream, int32_t num_splits,
-                  int64_t* trace) {
-  smla_status_t st =
-      validate(q, kv, idx, index_dtype, sink, scale, out, lse, T, H, num_kv, topk, trace);
+                  int64_t* trace, int32_t d_qk = smla::kHeadDim, int32_t d_v = smla::kHeadDim,
+                  bool fp8 = false, const float* kv_scale = nullptr) {
+  smla_status_t st = validate(q, kv, idx, index_dtype, sink, scale, out, lse, T, H, num_kv, topk,
+                              trace, d_qk, d_v, fp8 ? uint64_t(d_qk) : 0);
   if (st != SMLA_OK) return st;
+  // the tcgen05 kernel serves 512-wide bf16 rows only
+  const bool dims512 = d_qk == smla::kHeadDim && d_v == smla::kHeadDim && !fp8;
   Plan pl;
-  st = make_plan(T, H, topk, num_kv, num_splits, T > 0 ? device_sms() : kDefaultSMs, &pl);
+  st = make_plan(T, H, topk, num_kv, num_splits, T > 0 ? device_sms() : kDefaultSMs, &pl,
+                 dims512);
   if (st != SMLA_OK) return st;
   if (T == 0) return SMLA_OK;
 
@@ -161,6 +176,10 @@ smla_status_t run(const void* q, const void* kv, const void* idx, int32_t index_
   p.topk = topk;
   p.splits = pl.splits;
   p.idx64 = index_dtype == SMLA_IDX_INT64 ? 1 : 0;
+  p.d_qk = d_qk;
+  p.d_v = d_v;
+  p.kv_fp8 = fp8 ? 1 : 0;
+  p.kv_scale = kv_scale;
   p.scale = scale;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -176,12 +195,12 @@ smla_status_t run(const void* q, const void* kv, const void* idx, int32_t index_
   }
   // split path: stream-ordered workspace for the partials
   const uint64_t rows = uint64_t(pl.splits) * uint64_t(T) * uint64_t(H);
-  const size_t bytes = rows * smla::kHeadDim * 4 + rows * 4;
+  const size_t bytes = rows * d_v * 4 + rows * 4;
   void* ws = nullptr;
   cudaError_t ce = cudaMallocAsync(&ws, bytes, s);
   if (ce != cudaSuccess) return cuda_fail(ce, "cudaMallocAsync(split workspace)");
   p.part_o = static_cast<float*>(ws);
-  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + rows * smla::kHeadDim * 4);
+  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + rows * d_v * 4);
   int e = smla::launch_smallh(p, stream);
   if (e == 0) e = smla::launch_combine(p, stream);
   ce = cudaFreeAsync(ws, s);
@@ -370,6 +389,32 @@ smla_status_t sparse_mla_fwd(const void* q, const void* kv, const void* topk_ind
              stream, 0, nullptr);
 }
 
+smla_status_t sparse_mla_fwd_fp8kv(const void* q, const void* kv_fp8, const float* kv_scale,
+                                   const void* topk_indices, int32_t index_dtype,
+                                   const float* attn_sink, float scale, void* out, float* lse,
+                                   int64_t T, int32_t H, int64_t num_kv, int32_t topk,
+                                   void* stream) {
+  if (T < 0 || num_kv < 0 || num_kv >= (int64_t(1) << 31) || topk < 0) return SMLA_ERR_BAD_SHAPE;
+  if (T > 0 && num_kv > 0 && (kv_fp8 == nullptr || kv_scale == nullptr)) return SMLA_ERR_NULL_PTR;
+  if ((kv_fp8 && !aligned(kv_fp8, 16)) || (kv_scale && !aligned(kv_scale, 16)))
+    return SMLA_ERR_MISALIGNED;
+  // the scales are one more input that the outputs may not overlap
+  const uint64_t sb = uint64_t(num_kv) * 16;
+  const uint64_t ob = uint64_t(T) * H * smla::kHeadDim * 2, lb = uint64_t(T) * H * 4;
+  if (overlap(out, ob, kv_scale, sb) || overlap(lse, lb, kv_scale, sb)) return SMLA_ERR_ALIASING;
+  return run(q, kv_fp8, topk_indices, index_dtype, attn_sink, scale, out, lse, T, H, num_kv, topk,
+             stream, 0, nullptr, smla::kHeadDim, smla::kHeadDim, true, kv_scale);
+}
+
+smla_status_t sparse_mla_fwd_dims(const void* q, const void* kv, const void* topk_indices,
+                                  int32_t index_dtype, const float* attn_sink, float scale,
+                                  void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
+                                  int32_t topk, int32_t d_qk, int32_t d_v, void* stream) {
+  if (!smla::smallh_dims_supported(d_qk, d_v)) return SMLA_ERR_BAD_SHAPE;
+  return run(q, kv, topk_indices, index_dtype, attn_sink, scale, out, lse, T, H, num_kv, topk,
+             stream, 0, nullptr, d_qk, d_v);
+}
+
 smla_status_t sparse_mla_fwd_ex(const void* q, const void* kv, const void* topk_indices,
                                 int32_t index_dtype, const float* attn_sink, float scale,
                                 void* out, float* lse, int64_t T, int32_t H, int64_t num_kv,
@@ -408,9 +453,93 @@ smla_status_t sparse_mla_fwd_static_scratch(const void* q, const void* kv,
   p.topk = topk;
   p.splits = splits;
   p.idx64 = index_dtype == SMLA_IDX_INT64 ? 1 : 0;
+  p.d_qk = smla::kHeadDim;
+  p.d_v = smla::kHeadDim;
   p.scale = scale;
   const int e = smla::launch_split_static_scratch(p, stream);
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "static-scratch split path launch");
+  return SMLA_OK;
+}
+
+smla_status_t sparse_mla_bwd_workspace(int64_t T, int32_t H, int32_t topk, int64_t num_kv,
+                                       uint64_t* bytes) {
+  if (T < 0 || topk < 0 || topk > smla::kSmallHMaxSlots || num_kv < 0 ||
+      num_kv >= (int64_t(1) << 31) || T * int64_t(topk) >= (int64_t(1) << 31))
+    return SMLA_ERR_BAD_SHAPE;
+  if (!(H == 8 || H == 16 || H == 32 || H == 64 || H == 128)) return SMLA_ERR_UNSUPPORTED_H;
+  if (bytes == nullptr) return SMLA_ERR_NULL_PTR;
+  *bytes = smla::bwd_workspace_layout(T, H, topk, num_kv).total;
+  return SMLA_OK;
+}
+
+smla_status_t sparse_mla_bwd(const void* q, const void* kv, const void* topk_indices,
+                             int32_t index_dtype, const float* attn_sink, float scale,
+                             const void* out, const float* lse, const void* dout, float* dq,
+                             float* dkv, float* dsink, int64_t T, int32_t H, int64_t num_kv,
+                             int32_t topk, void* workspace, uint64_t workspace_bytes,
+                             void* stream) {
+  uint64_t need = 0;
+  smla_status_t st = sparse_mla_bwd_workspace(T, H, topk, num_kv, &need);
+  if (st != SMLA_OK) return st;
+  if (index_dtype != SMLA_IDX_INT32 && index_dtype != SMLA_IDX_INT64)
+    return SMLA_ERR_BAD_INDEX_DTYPE;
+  if (!std::isfinite(scale)) return SMLA_ERR_BAD_SCALE;
+  if (num_kv > 0 && (kv == nullptr || dkv == nullptr)) return SMLA_ERR_NULL_PTR;
+  if (T > 0 && (q == nullptr || out == nullptr || lse == nullptr || dout == nullptr ||
+                dq == nullptr || (topk > 0 && topk_indices == nullptr)))
+    return SMLA_ERR_NULL_PTR;
+  const uintptr_t isz = index_dtype == SMLA_IDX_INT64 ? 8 : 4;
+  if ((q && !aligned(q, 16)) || (kv && !aligned(kv, 16)) || (out && !aligned(out, 16)) ||
+      (dout && !aligned(dout, 16)) || (dq && !aligned(dq, 16)) || (dkv && !aligned(dkv, 16)) ||
+      (lse && !aligned(lse, 4)) || (dsink && !aligned(dsink, 4)) ||
+      (attn_sink && !aligned(attn_sink, 4)) || (topk_indices && !aligned(topk_indices, isz)))
+    return SMLA_ERR_MISALIGNED;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
+    return SMLA_ERR_WORKSPACE;
+  const uint64_t qb = uint64_t(T) * H * smla::kHeadDim * 2;
+  const uint64_t kvb = uint64_t(num_kv) * smla::kHeadDim * 2;
+  const uint64_t ib = uint64_t(T) * topk * isz;
+  const uint64_t lb = uint64_t(T) * H * 4;
+  const uint64_t sb = attn_sink ? uint64_t(H) * 4 : 0;
+  const void* ins[6] = {q, kv, topk_indices, attn_sink, out, dout};
+  const uint64_t inb[6] = {qb, kvb, ib, sb, qb, qb};
+  void* outs[4] = {dq, dkv, dsink, workspace};
+  const uint64_t outb[4] = {qb * 2, kvb * 2, dsink ? uint64_t(H) * 4 : 0, need};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 6; ++i)
+      if (overlap(outs[o], outb[o], ins[i], inb[i])) return SMLA_ERR_ALIASING;
+    if (overlap(outs[o], outb[o], lse, lb)) return SMLA_ERR_ALIASING;
+    for (int o2 = o + 1; o2 < 4; ++o2)
+      if (overlap(outs[o], outb[o], outs[o2], outb[o2])) return SMLA_ERR_ALIASING;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (T == 0) {   // no token: every gradient is zero
+    if (num_kv > 0 && (e = cudaMemsetAsync(dkv, 0, kvb * 2, s)) != cudaSuccess)
+      return cuda_fail(e, "zero dkv");
+    if (dsink && (e = cudaMemsetAsync(dsink, 0, uint64_t(H) * 4, s)) != cudaSuccess)
+      return cuda_fail(e, "zero dsink");
+    return SMLA_OK;
+  }
+  smla::BwdParams p{};
+  p.q = q;
+  p.kv = kv;
+  p.idx = topk_indices;
+  p.sink = attn_sink;
+  p.out = out;
+  p.lse = lse;
+  p.dout = dout;
+  p.dq = dq;
+  p.dkv = dkv;
+  p.dsink = dsink;
+  p.T = T;
+  p.num_kv = num_kv;
+  p.H = H;
+  p.topk = topk;
+  p.idx64 = index_dtype == SMLA_IDX_INT64 ? 1 : 0;
+  p.scale = scale;
+  const int r = smla::launch_bwd(p, workspace, stream);
+  if (r != 0) return cuda_fail(static_cast<cudaError_t>(r), "backward launch");
   return SMLA_OK;
 }
 
@@ -439,7 +568,8 @@ smla_status_t sparse_mla_launch_config(int64_t T, int32_t H, int32_t topk, int64
   if (st != SMLA_OK) return st;
   smla::LaunchGeom g{0, 0, 0, 0};
   const int e = pl.family == 1 ? smla::h128_geometry(T, &g)
-                               : smla::smallh_geometry(T, H, pl.splits, &g);
+                               : smla::smallh_geometry(T, H, pl.splits, smla::kHeadDim,
+                                                       smla::kHeadDim, &g);
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "launch geometry");
   if (grid_ctas) *grid_ctas = g.grid_ctas;
   if (cta_threads) *cta_threads = g.threads;

@@ -14,8 +14,8 @@
 // A row whose M is -inf (no valid slot anywhere, no finite sink) gives O = 0,
 // lse = -inf; an empty split has weight exp(-inf) = 0, never NaN.
 //
-// One warp per (token, head): 32 lanes x 16 columns, fp32 partials read as
-// float4, bf16 output written as 2 x 16 bytes per lane.
+// One warp per (token, head): 32 lanes x d_v/32 columns (16 at d_v = 512: fp32
+// partials read as float4, bf16 output written as 2 x 16 bytes per lane).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -28,7 +28,14 @@ namespace {
 
 constexpr int kRowsPerBlock = 8;
 
+// kDv output columns per row: each lane owns kC = kDv / 32 consecutive columns.
+template <int kDv>
 __global__ void __launch_bounds__(kRowsPerBlock * 32) combine_kernel(const FwdParams p) {
+  // launched as a programmatic dependent of the split kernel: wait until that
+  // grid has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kC = kDv / 32;
+  static_assert(kC % 2 == 0, "pairs of columns per lane");
   const int lane = threadIdx.x & 31;
   const int64_t TH = p.T * p.H;
   const int64_t row = int64_t(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
@@ -42,50 +49,88 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) combine_kernel(const FwdPa
     sk = p.sink[h] * kLog2e;
     M = fmaxf(M, sk);
   }
-  uint4* out = reinterpret_cast<uint4*>(static_cast<char*>(p.out) + row * int64_t(kHeadDim * 2));
-  if (M == -INFINITY) {
-    out[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-    out[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-    if (lane == 0) p.lse[row] = -INFINITY;
-    return;
-  }
-  float acc[16];
+  uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<char*>(p.out) + row * int64_t(kDv * 2)) +
+                  lane * (kC / 2);
+  float acc[kC];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int i = 0; i < kC; ++i) acc[i] = 0.f;
   float den = 0.f;
-  for (int s = 0; s < p.splits; ++s) {
-    const int64_t prow = int64_t(s) * TH + row;
-    const float w = ex2(p.part_lse[prow] * kLog2e - M);
-    den += w;
-    if (w == 0.f) continue;   // empty split (or negligible): skip its partial
-    const float4* po = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim) + lane * 4;
+  if (M != -INFINITY) {
+    for (int s = 0; s < p.splits; ++s) {
+      const int64_t prow = int64_t(s) * TH + row;
+      const float w = ex2(p.part_lse[prow] * kLog2e - M);
+      den += w;
+      if (w == 0.f) continue;   // empty split (or negligible): skip its partial
+      const float* po = p.part_o + prow * kDv + lane * kC;
+      if constexpr (kC % 4 == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 v = po[i];
-      acc[4 * i + 0] += w * v.x; acc[4 * i + 1] += w * v.y;
-      acc[4 * i + 2] += w * v.z; acc[4 * i + 3] += w * v.w;
+        for (int i = 0; i < kC / 4; ++i) {
+          const float4 v = reinterpret_cast<const float4*>(po)[i];
+          acc[4 * i + 0] += w * v.x; acc[4 * i + 1] += w * v.y;
+          acc[4 * i + 2] += w * v.z; acc[4 * i + 3] += w * v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kC / 2; ++i) {
+          const float2 v = reinterpret_cast<const float2*>(po)[i];
+          acc[2 * i] += w * v.x; acc[2 * i + 1] += w * v.y;
+        }
+      }
     }
+    if (p.sink != nullptr) den += ex2(sk - M);
   }
-  if (p.sink != nullptr) den += ex2(sk - M);
-  const float f = 1.f / den;
-  uint4 o0, o1;
-  o0.x = pack_bf16x2(acc[0] * f, acc[1] * f);   o0.y = pack_bf16x2(acc[2] * f, acc[3] * f);
-  o0.z = pack_bf16x2(acc[4] * f, acc[5] * f);   o0.w = pack_bf16x2(acc[6] * f, acc[7] * f);
-  o1.x = pack_bf16x2(acc[8] * f, acc[9] * f);   o1.y = pack_bf16x2(acc[10] * f, acc[11] * f);
-  o1.z = pack_bf16x2(acc[12] * f, acc[13] * f); o1.w = pack_bf16x2(acc[14] * f, acc[15] * f);
-  out[2 * lane] = o0;
-  out[2 * lane + 1] = o1;
-  if (lane == 0) p.lse[row] = (M + log2f(den)) * kLn2;
+  // a row whose M is -inf (nothing valid, no finite sink): O = 0, lse = -inf
+  const float f = (M == -INFINITY) ? 0.f : 1.f / den;
+  uint32_t w[kC / 2];
+#pragma unroll
+  for (int i = 0; i < kC / 2; ++i) w[i] = pack_bf16x2(acc[2 * i] * f, acc[2 * i + 1] * f);
+  if constexpr (kC % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < kC / 8; ++i)
+      reinterpret_cast<uint4*>(out)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  } else if constexpr (kC % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < kC / 4; ++i) reinterpret_cast<uint2*>(out)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kC / 2; ++i) out[i] = w[i];
+  }
+  if (lane == 0) p.lse[row] = (M == -INFINITY) ? -INFINITY : (M + log2f(den)) * kLn2;
+}
+
+template <int kDv>
+cudaError_t launch_dv(const FwdParams& p, cudaStream_t stream) {
+  const int64_t rows = p.T * p.H;
+  const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kRowsPerBlock * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel<kDv>, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace
 
+// Launched with programmatic stream serialization: its CTAs may be scheduled
+// while the split kernel still runs (that kernel signals it at its start) and
+// wait in griddepcontrol.wait, so a decode-sized call does not pay a second
+// launch latency.
 int launch_combine(const FwdParams& p, void* stream) {
-  const int64_t rows = p.T * p.H;
-  const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-  combine_kernel<<<static_cast<unsigned>(blocks), kRowsPerBlock * 32, 0,
-                   static_cast<cudaStream_t>(stream)>>>(p);
-  return static_cast<int>(cudaGetLastError());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (p.d_v) {
+    case 512: return static_cast<int>(launch_dv<512>(p, s));
+    case 128: return static_cast<int>(launch_dv<128>(p, s));
+    case 576: return static_cast<int>(launch_dv<576>(p, s));
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
 }
 
 }  // namespace smla

@@ -245,7 +245,7 @@ __device__ __forceinline__ void land_and_arrive(uint32_t bar) {
 // with 2-D TMA once the previous token's last S has completed (the MMA thread
 // copies them into TMEM and loads columns 128-255) and prefetches the next
 // token's Q into L2.
-template <typename IdxT>
+template <typename IdxT, bool kTrace>
 __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, const CUtensorMap* tm_o,
                               uint8_t* base, Bars* b, uint32_t tmem, uint32_t rank, int warp,
                               int lane) {
@@ -255,7 +255,9 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
   const char* kvb = reinterpret_cast<const char*>(p.kv) + 512 * rank;   // this CTA's half
   const int c = lane;                                  // 16-byte chunk of the half row
   const uint32_t chunk_off = (c >> 3) * 8192;          // its 64-column block
-  const bool trace = p.trace != nullptr && rank == 0;
+  // the read trace exists only in the instantiation built for it, so that the
+  // production gather loop carries no trace code
+  const bool trace = kTrace && rank == 0;
   uint32_t gt = 0, qn = 0, q_loads = 0;
   int it = 0;
 
@@ -433,8 +435,8 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
             const char* src = valid ? kvb + int64_t(rr) * 1024 + c * 16 : kvb;
             cp_async_16(dst + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
             // read trace: the row this copy reads, recovered from its source address
-            if (trace && c == 0 && valid)
-              p.trace[tok * p.topk + j * kTileN + r] = (src - kvb) >> 10;
+            if constexpr (kTrace)
+              if (trace && c == 0 && valid) p.trace[tok * p.topk + j * kTileN + r] = (src - kvb) >> 10;
           }
         }
         cp_async_commit();
@@ -893,7 +895,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
   }
 }
 
-template <typename IdxT>
+template <typename IdxT, bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1)
     h128_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                     const H128Params p) {
@@ -950,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = b->tmem_base;
 
   if (warp < kMmaWarp) {
-    producer_role<IdxT>(p, &tm_q, &tm_o, base, b, tmem, rank, warp, lane);
+    producer_role<IdxT, kTrace>(p, &tm_q, &tm_o, base, b, tmem, rank, warp, lane);
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role(p, base, b, tmem, &tm_q, rank);
     __syncwarp();
@@ -1018,9 +1020,9 @@ cudaLaunchConfig_t launch_config(unsigned ctas, cudaStream_t stream, cudaLaunchA
   return cfg;
 }
 
-template <typename IdxT>
+template <typename IdxT, bool kTrace>
 cudaError_t prepare(DeviceState& st) {
-  auto kern = h128_fwd_kernel<IdxT>;
+  auto kern = h128_fwd_kernel<IdxT, kTrace>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
@@ -1039,7 +1041,7 @@ constexpr int kMaxDev = 64;
 
 // Per-device, per-instantiation launch state (shared-memory attribute set,
 // co-resident cluster count), prepared on first use.
-template <typename IdxT>
+template <typename IdxT, bool kTrace>
 cudaError_t device_state(DeviceState** out) {
   static DeviceState states[kMaxDev];
   static std::mutex mu;
@@ -1048,15 +1050,15 @@ cudaError_t device_state(DeviceState** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!states[dev].ready && (e = prepare<IdxT>(states[dev])) != cudaSuccess) return e;
+  if (!states[dev].ready && (e = prepare<IdxT, kTrace>(states[dev])) != cudaSuccess) return e;
   *out = &states[dev];
   return cudaSuccess;
 }
 
-template <typename IdxT>
+template <typename IdxT, bool kTrace>
 cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   DeviceState* st = nullptr;
-  cudaError_t e = device_state<IdxT>(&st);
+  cudaError_t e = device_state<IdxT, kTrace>(&st);
   if (e != cudaSuccess) return e;
   CUtensorMap tq, to;
   if (!make_map(&tq, fp.q, static_cast<uint64_t>(fp.T) * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1081,7 +1083,7 @@ cudaError_t launch_typed(const FwdParams& fp, cudaStream_t stream) {
   const int64_t clusters = fp.T < st->max_clusters ? fp.T : st->max_clusters;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(static_cast<unsigned>(2 * clusters), stream, attr);
-  e = cudaLaunchKernelEx(&cfg, h128_fwd_kernel<IdxT>, tq, to, p);
+  e = cudaLaunchKernelEx(&cfg, h128_fwd_kernel<IdxT, kTrace>, tq, to, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1120,13 +1122,15 @@ bool h128_supported(int64_t T, int32_t H, int32_t topk, int64_t num_kv) {
 
 int launch_h128(const FwdParams& p, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = p.idx64 ? launch_typed<int64_t>(p, s) : launch_typed<int32_t>(p, s);
+  const bool tr = p.trace != nullptr;
+  const cudaError_t e = p.idx64 ? (tr ? launch_typed<int64_t, true>(p, s) : launch_typed<int64_t, false>(p, s))
+                                : (tr ? launch_typed<int32_t, true>(p, s) : launch_typed<int32_t, false>(p, s));
   return static_cast<int>(e);
 }
 
 int h128_geometry(int64_t T, LaunchGeom* g) {
   DeviceState* st = nullptr;
-  const cudaError_t e = device_state<int32_t>(&st);
+  const cudaError_t e = device_state<int32_t, false>(&st);
   if (e != cudaSuccess) return static_cast<int>(e);
   const int64_t clusters = T < st->max_clusters ? T : st->max_clusters;
   g->grid_ctas = static_cast<int>(2 * clusters);

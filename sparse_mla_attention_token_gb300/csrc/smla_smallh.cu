@@ -27,6 +27,24 @@
 //
 // Split mode (splits > 1): each slot range writes its sink-free partial
 // (O normalised by its own sum, lse of its own slots) for the combine kernel.
+//
+// Head dims: the kernel is instantiated for score width kDqk in {128, 512,
+// 576} (kDqk / 64 warps, one 64-column slice each) and value width kDv <= kDqk
+// (the first kDv columns of each gathered row; kDv = 512 with kDqk = 576 is the
+// MLA layout whose last 64 columns are a positional part used in the scores
+// only: "Add DSv4 sparse MLA prefill Triton and unified with MLA Gluon kernel
+// on GFX950", the has_pe flag; head dims 128 and 576: "Tuned sparse MLA
+// prefill for DSv4.1-Flash TP4", its tests).
+//
+// fp8 cache (kFp8, 512 columns): each kv row is 512 e4m3 bytes and 4 fp32
+// scales, one per 128-column block (value = code * scale).  The gather moves
+// the 512 + 16 bytes with cp.async into an fp8 ring; at the start of each tile
+// the CTA decodes the codes exactly into the bf16 stage (e4m3 is a subset of
+// bf16); the scales are applied in fp32: to each warp's partial scores (a warp's
+// 64 columns lie in one block) and to the probabilities, one bf16 copy of P per
+// block, so that P.V and the scores see code * scale without a second rounding
+// of the values.
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -39,42 +57,84 @@
 namespace smla {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
 constexpr int kHG = 16;           // heads per CTA (mma M)
-constexpr int kOStride = 520;     // bf16 per row of the staged output tile (bank spread)
-constexpr int kRowBytes = kHeadDim * 2;
-
-// 32 gathered rows per tile: ~95 KB of shared memory and at most 128
-// registers, so two CTAs share an SM and hide each other's gather latency
-// (measured faster than 64-row tiles at one CTA per SM for every slot count).
+// 32 gathered rows per tile: ~95 KB of shared memory at 512 columns and at
+// most 128 registers, so two CTAs share an SM and hide each other's gather
+// latency (measured faster than 64-row tiles at one CTA per SM for every slot
+// count).
 constexpr int kBN = 32;
+
+// Shape constants of one (score width, value width) instantiation.
+template <int kDqk, int kDv>
+struct Dims {
+  static_assert(kDqk % 64 == 0 && kDv % 64 == 0 && kDv <= kDqk, "64-column slices");
+  static constexpr int kWarps = kDqk / 64;          // one 64-column slice of the scores each
+  static constexpr int kVWarps = kDv / 64;          // warps that also own value columns
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kRowBytes = kDqk * 2;        // one gathered row
+  static constexpr int kOStride = kDv + 8;          // bf16 per row of the staged output tile
+  static constexpr int kHW = 2 * kWarps;            // half-warps; one owns a softmax row at a time
+  static constexpr int kRowsPerHW = (kHG + kHW - 1) / kHW;
+  static constexpr int kMinBlocks = kDqk <= 512 ? 2 : 1;
+};
+
+// Shared memory of the bf16 instantiations: two bf16 stages of the gather ring.
+template <int kDqk, int kDv, bool kFp8 = false>
 struct __align__(128) Smem {
+  using Dm = Dims<kDqk, kDv>;
   static constexpr int kSredStride = kBN + 8;   // floats per row of a warp's partial scores
   static constexpr int kPStride = kBN + 8;      // bf16 per row of P (bank spread for ldmatrix)
-  __nv_bfloat16 kv[2][kBN * kHeadDim];     // 2 stages; 16 B chunk c of row r at c ^ (r & 7)
-  float sred[kWarps][kHG * kSredStride];   // per-warp partial scores
-  __nv_bfloat16 p[kHG * kPStride];         // probabilities, A operand of P.V
+  __nv_bfloat16 kv[2][kBN * kDqk];         // 2 stages; 16 B chunk c of row r at c ^ (r & 7)
+  float sred[Dm::kWarps][kHG * kSredStride];   // per-warp partial scores
+  __nv_bfloat16 p[1][kHG * kPStride];      // probabilities, A operand of P.V
   float alpha[kHG];                        // per-row rescale of O for the current tile
   float row_m[kHG];                        // final running max (log2 units)
   float row_l[kHG];                        // final running sum
   int rows[2][kSmallHMaxSlots];            // compacted valid kv rows, slot order (this token, next)
-  int warp_cnt[kWarps];
+  int warp_cnt[Dm::kWarps];
+  static_assert(sizeof(kv[0]) >= kHG * Dm::kOStride * 2, "output staging fits one stage");
 };
-static_assert(sizeof(Smem::kv[0]) >= kHG * kOStride * 2, "output staging fits one stage");
 
+// The fp8-cache instantiation: a two-stage ring of raw e4m3 rows and their
+// scales, decoded tile by tile into one bf16 stage.
+template <>
+struct __align__(128) Smem<512, 512, true> {
+  using Dm = Dims<512, 512>;
+  static constexpr int kSredStride = kBN + 8;
+  static constexpr int kPStride = kBN + 8;
+  __nv_bfloat16 kv[1][kBN * 512];          // the decoded tile (same layout as a bf16 stage)
+  float sred[Dm::kWarps][kHG * kSredStride];
+  __nv_bfloat16 p[4][kHG * kPStride];      // P times each 128-column block's scale
+  float alpha[kHG];
+  float row_m[kHG];
+  float row_l[kHG];
+  int rows[2][kSmallHMaxSlots];
+  int warp_cnt[Dm::kWarps];
+  uint8_t f8[2][kBN * 512];                // fp8 ring: raw e4m3 rows
+  float scl[2][kBN][4];                    // their block scales
+  static_assert(sizeof(kv[0]) >= kHG * Dm::kOStride * 2, "output staging fits one stage");
+};
+
+template <int kRowBytes>
 __device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t base, int r, int c) {
   return base + r * kRowBytes + ((c ^ (r & 7)) << 4);
 }
 
-template <typename IdxT, bool kSplit>
-__global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams p) {
+// kTrace: the instantiation that writes the read trace (p.trace); the others
+// carry no trace code in their gather loop.  kFp8: kv is the fp8 cache.
+template <typename IdxT, bool kSplit, int kDqk, int kDv, bool kTrace, bool kFp8 = false>
+__global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kMinBlocks)
+    smallh_fwd_kernel(const FwdParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  using SmemT = Smem;
+  using Dm = Dims<kDqk, kDv>;
+  using SmemT = Smem<kDqk, kDv, kFp8>;
+  constexpr int kWarps = Dm::kWarps, kThreads = Dm::kThreads, kRowBytes = Dm::kRowBytes;
+  constexpr int kOStride = Dm::kOStride, kHW = Dm::kHW, kRPH = Dm::kRowsPerHW;
   constexpr int kSredStride = SmemT::kSredStride, kPStride = SmemT::kPStride;
   constexpr int kNT = kBN / 8;     // 8-slot n-tiles of S
   constexpr int kCols = kBN / 16;  // softmax columns per lane (16 lanes per row)
   SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  const auto kv_chunk = [](uint32_t base, int r, int c) { return kv_chunk_addr<kRowBytes>(base, r, c); };
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -91,21 +151,24 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
   const int j0 = min(p.topk, split * chunk);
   const int j1 = min(p.topk, j0 + chunk);
   const int64_t t0 = blockIdx.x, tstride = gridDim.x;   // tokens t0, t0 + tstride, ...
+  // the combine kernel that follows a split launch may be scheduled now: it
+  // waits for this whole grid to finish before it reads a partial
+  if constexpr (kSplit) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (t0 >= p.T) return;
 
   // this warp's Q fragments of token t: rows = heads of the group, k = its 64 columns
   uint32_t qa[4][4];
   auto load_q = [&](int64_t t) {
     const uint32_t* q32 = static_cast<const uint32_t*>(p.q);
-    const int64_t rbase = (t * H + h0) * kHeadDim;
+    const int64_t rbase = (t * H + h0) * kDqk;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const int d = warp * 64 + kk * 16 + 2 * tig;
       const bool lo = g < hvalid, hi = (g + 8) < hvalid;
-      qa[kk][0] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d) >> 1] : 0u;
-      qa[kk][1] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d) >> 1] : 0u;
-      qa[kk][2] = lo ? q32[(rbase + int64_t(g) * kHeadDim + d + 8) >> 1] : 0u;
-      qa[kk][3] = hi ? q32[(rbase + int64_t(g + 8) * kHeadDim + d + 8) >> 1] : 0u;
+      qa[kk][0] = lo ? q32[(rbase + int64_t(g) * kDqk + d) >> 1] : 0u;
+      qa[kk][1] = hi ? q32[(rbase + int64_t(g + 8) * kDqk + d) >> 1] : 0u;
+      qa[kk][2] = lo ? q32[(rbase + int64_t(g) * kDqk + d + 8) >> 1] : 0u;
+      qa[kk][3] = hi ? q32[(rbase + int64_t(g + 8) * kDqk + d + 8) >> 1] : 0u;
     }
   };
 
@@ -140,32 +203,53 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
     }
     // read trace: the range's entries past its valid count are never read (-1);
     // the gather writes the others
-    if (p.trace != nullptr && hg == 0)
-      for (int k = j0 + nvalid + tid; k < j1; k += kThreads) p.trace[t * p.topk + k] = -1;
+    if constexpr (kTrace)
+      if (hg == 0)
+        for (int k = j0 + nvalid + tid; k < j1; k += kThreads) p.trace[t * p.topk + k] = -1;
     return nvalid;
   };
 
   const char* kvb = static_cast<const char*>(p.kv);
   // gather tile `tile` of token t's rows in list `buf` (count nvalid) into `stage`
   auto issue_tile = [&](int64_t t, int buf, int nvalid, int tile, int stage) {
-    const uint32_t dst0 = smem_u32(sm.kv[stage]);
     const int* rows = sm.rows[buf];
+    if constexpr (kFp8) {
+      // 32 chunks of codes and one chunk of scales per row; the tail zero-filled
+      const uint32_t f0 = smem_u32(sm.f8[stage]), s0 = smem_u32(sm.scl[stage]);
+      const uint8_t* cb = static_cast<const uint8_t*>(p.kv);
+      const char* sb = reinterpret_cast<const char*>(p.kv_scale);
 #pragma unroll 4
-    for (int i = tid; i < kBN * 64; i += kThreads) {
-      const int r = i >> 6, c = i & 63;
+      for (int i = tid; i < kBN * 33; i += kThreads) {
+        const int r = i / 33, c = i % 33;
+        const int slot = tile * kBN + r;
+        const bool ok = slot < nvalid;
+        const int64_t row = ok ? rows[slot] : 0;
+        if (c < 32)
+          cp_async_16(f0 + r * 512 + c * 16, cb + row * 512 + c * 16, ok ? 16u : 0u);
+        else
+          cp_async_16(s0 + r * 16, sb + row * 16, ok ? 16u : 0u);
+      }
+      cp_async_commit();
+      return;
+    }
+    const uint32_t dst0 = smem_u32(sm.kv[stage]);
+    constexpr int kChunks = kRowBytes / 16;   // 16-byte chunks per gathered row
+#pragma unroll 4
+    for (int i = tid; i < kBN * kChunks; i += kThreads) {
+      const int r = i / kChunks, c = i % kChunks;
       const int slot = tile * kBN + r;
       const bool ok = slot < nvalid;
       const char* src = ok ? kvb + int64_t(rows[slot]) * kRowBytes + c * 16 : kvb;
-      cp_async_16(kv_chunk_addr(dst0, r, c), src, ok ? 16u : 0u);
+      cp_async_16(kv_chunk(dst0, r, c), src, ok ? 16u : 0u);
       // read trace: the row this copy reads, recovered from its source address
-      if (p.trace != nullptr && hg == 0 && c == 0 && ok)
-        p.trace[t * p.topk + j0 + slot] = (src - kvb) / kRowBytes;
+      if constexpr (kTrace)
+        if (hg == 0 && c == 0 && ok) p.trace[t * p.topk + j0 + slot] = (src - kvb) / kRowBytes;
     }
     cp_async_commit();
   };
 
   const float sl2 = p.scale * kLog2e;
-  const int srow = 2 * warp + (lane >> 4);   // softmax row owned by this half-warp
+  const int hw = 2 * warp + (lane >> 4);     // half-warp: owns softmax rows hw, hw + kHW, ...
   const int sc0 = (lane & 15) * kCols;       // its kCols columns
 
   // The CTA's tokens run as one stream of tiles through the two-stage ring:
@@ -183,7 +267,12 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
     const int ntiles = (nv_cur + kBN - 1) / kBN;
     int nv_next = 0;
     bool next_done = false;       // the next token's list compacted (and its tile issued)
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run[kRPH], l_run[kRPH];
+#pragma unroll
+    for (int i = 0; i < kRPH; ++i) {
+      m_run[i] = -INFINITY;
+      l_run[i] = 0.f;
+    }
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -199,7 +288,30 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
         next_done = true;
         if (nv_next > 0) issue_tile(tn, cur ^ 1, nv_next, 0, stage ^ 1);
       }
-      const uint32_t kvs = smem_u32(sm.kv[stage]);
+      if constexpr (kFp8) {
+        // decode the tile's e4m3 codes exactly into the bf16 stage (4 x 16 codes
+        // per thread); every warp finished the previous tile's P.V (barrier above)
+        const uint32_t kv0 = smem_u32(sm.kv[0]);
+#pragma unroll
+        for (int k = 0; k < kBN * 32 / kThreads; ++k) {
+          const int i = tid + k * kThreads, r = i >> 5, c = i & 31;
+          const uint4 raw = *reinterpret_cast<const uint4*>(&sm.f8[stage][r * 512 + c * 16]);
+          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const __nv_fp8x2_storage_t two =
+                static_cast<__nv_fp8x2_storage_t>((w4[j >> 1] >> (16 * (j & 1))) & 0xffffu);
+            const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+            o[j] = pack_bf16x2(__half2float(__half(__half_raw{h.x})),
+                               __half2float(__half(__half_raw{h.y})));
+          }
+          sts_u4(kv_chunk(kv0, r, 2 * c), make_uint4(o[0], o[1], o[2], o[3]));
+          sts_u4(kv_chunk(kv0, r, 2 * c + 1), make_uint4(o[4], o[5], o[6], o[7]));
+        }
+        __syncthreads();
+      }
+      const uint32_t kvs = smem_u32(sm.kv[kFp8 ? 0 : stage]);
       // ---- 3. partial S over this warp's 64 columns
       float s[kNT][4];
   #pragma unroll
@@ -211,9 +323,18 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
         for (int nt = 0; nt < kNT; ++nt) {
           const int r = nt * 8 + (lane & 7);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kv_chunk_addr(kvs, r, c), b0, b1, b2, b3);
+          ldmatrix_x4(kv_chunk(kvs, r, c), b0, b1, b2, b3);
           mma_16816(s[nt], qa[2 * kp], b0, b1);
           mma_16816(s[nt], qa[2 * kp + 1], b2, b3);
+        }
+      }
+      if constexpr (kFp8) {
+        // this warp's 64 columns lie in scale block warp / 2: scale each slot's partial
+  #pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          const float c0 = sm.scl[stage][nt * 8 + 2 * tig][warp >> 1];
+          const float c1 = sm.scl[stage][nt * 8 + 2 * tig + 1][warp >> 1];
+          s[nt][0] *= c0; s[nt][1] *= c1; s[nt][2] *= c0; s[nt][3] *= c1;
         }
       }
       float* sw = sm.sred[warp];
@@ -226,8 +347,11 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
       }
       __syncthreads();
 
-      // ---- 4. reduce the 8 partials, online softmax (base 2)
-      {
+      // ---- 4. reduce the kWarps partials, online softmax (base 2)
+#pragma unroll
+      for (int ri = 0; ri < kRPH; ++ri) {
+        const int srow = hw + ri * kHW;
+        if (srow >= kHG) break;   // warp-uniform: kHW divides 16, or whole warps have no row
         float a[kCols];
   #pragma unroll
         for (int k = 0; k < kCols; ++k) a[k] = 0.f;
@@ -252,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
         }
   #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float m_new = fmaxf(m_run, mx);  // finite: the tile holds >= 1 valid row
-        const float alpha = ex2(m_run - m_new);
+        const float m_new = fmaxf(m_run[ri], mx);  // finite: the tile holds >= 1 valid row
+        const float alpha = ex2(m_run[ri] - m_new);
         float ps = 0.f;
   #pragma unroll
         for (int k = 0; k < kCols; ++k) {
@@ -262,24 +386,34 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
         }
   #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        l_run = l_run * alpha + ps;
-        m_run = m_new;
+        l_run[ri] = l_run[ri] * alpha + ps;
+        m_run[ri] = m_new;
+        if constexpr (kFp8) {
+          // P times each block's scale of the slot: the A operand of that block's warps
   #pragma unroll
-        for (int k = 0; k < kCols; k += 2)
-          *reinterpret_cast<uint32_t*>(&sm.p[srow * kPStride + sc0 + k]) = pack_bf16x2(x[k], x[k + 1]);
+          for (int b = 0; b < 4; ++b)
+  #pragma unroll
+            for (int k = 0; k < kCols; k += 2)
+              *reinterpret_cast<uint32_t*>(&sm.p[b][srow * kPStride + sc0 + k]) =
+                  pack_bf16x2(x[k] * sm.scl[stage][sc0 + k][b], x[k + 1] * sm.scl[stage][sc0 + k + 1][b]);
+        } else {
+  #pragma unroll
+          for (int k = 0; k < kCols; k += 2)
+            *reinterpret_cast<uint32_t*>(&sm.p[0][srow * kPStride + sc0 + k]) = pack_bf16x2(x[k], x[k + 1]);
+        }
         if ((lane & 15) == 0) sm.alpha[srow] = alpha;
       }
       __syncthreads();
 
-      // ---- 5. O = alpha * O + P . V over this warp's 64 columns
-      {
+      // ---- 5. O = alpha * O + P . V over this warp's 64 columns (value warps)
+      if (warp < Dm::kVWarps) {
         const float a_lo = sm.alpha[g], a_hi = sm.alpha[g + 8];
   #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           acc[nt][0] *= a_lo; acc[nt][1] *= a_lo;
           acc[nt][2] *= a_hi; acc[nt][3] *= a_hi;
         }
-        const uint32_t ps = smem_u32(sm.p);
+        const uint32_t ps = smem_u32(sm.p[kFp8 ? warp >> 1 : 0]);
   #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
           uint32_t pa[4];
@@ -292,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
             const int r = ks * 16 + (j & 1) * 8 + (lane & 7);
             const int c = warp * 8 + np * 2 + (j >> 1);
             uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(kv_chunk_addr(kvs, r, c), b0, b1, b2, b3);
+            ldmatrix_x4_trans(kv_chunk(kvs, r, c), b0, b1, b2, b3);
             mma_16816(acc[2 * np], pa, b0, b1);
             mma_16816(acc[2 * np + 1], pa, b2, b3);
           }
@@ -301,9 +435,13 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
     }
 
     // ---- epilogue of token t
-    if ((lane & 15) == 0) {
-      sm.row_m[srow] = m_run;
-      sm.row_l[srow] = l_run;
+#pragma unroll
+    for (int ri = 0; ri < kRPH; ++ri) {
+      const int srow = hw + ri * kHW;
+      if ((lane & 15) == 0 && srow < kHG) {
+        sm.row_m[srow] = m_run[ri];
+        sm.row_l[srow] = l_run[ri];
+      }
     }
     __syncthreads();
 
@@ -317,18 +455,20 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
         const float m = sm.row_m[r], l = sm.row_l[r];
         const float f = (l > 0.f) ? 1.f / l : 0.f;
         const int64_t rowid = int64_t(split) * TH + t * H + h0 + r;
-        float* po = p.part_o + rowid * kHeadDim + warp * 64 + 2 * tig;
+        if (warp < Dm::kVWarps) {
+          float* po = p.part_o + rowid * kDv + warp * 64 + 2 * tig;
   #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-          *reinterpret_cast<float2*>(po + nt * 8) =
-              make_float2(acc[nt][2 * half] * f, acc[nt][2 * half + 1] * f);
+          for (int nt = 0; nt < 8; ++nt)
+            *reinterpret_cast<float2*>(po + nt * 8) =
+                make_float2(acc[nt][2 * half] * f, acc[nt][2 * half + 1] * f);
+        }
         if (warp == 0 && tig == 0) p.part_lse[rowid] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
       }
     } else {
       // fold the sink once, normalise, round to bf16, stage, store 16 B per thread
       // staged in the stage of the token's last tile: every warp has finished
       // reading it (barrier above); the next token's first tile is in the other one
-      __nv_bfloat16* ost = sm.kv[(gt - 1) & 1];
+      __nv_bfloat16* ost = sm.kv[kFp8 ? 0 : (gt - 1) & 1];
   #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int r = g + half * 8;
@@ -341,18 +481,21 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
         }
         const bool live = (m2 != -INFINITY) && (l2 > 0.f);
         const float f = live ? ex2(m - m2) / l2 : 0.f;
+        if (warp < Dm::kVWarps) {
   #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-          *reinterpret_cast<uint32_t*>(&ost[r * kOStride + warp * 64 + nt * 8 + 2 * tig]) =
-              pack_bf16x2(acc[nt][2 * half] * f, acc[nt][2 * half + 1] * f);
+          for (int nt = 0; nt < 8; ++nt)
+            *reinterpret_cast<uint32_t*>(&ost[r * kOStride + warp * 64 + nt * 8 + 2 * tig]) =
+                pack_bf16x2(acc[nt][2 * half] * f, acc[nt][2 * half + 1] * f);
+        }
         if (warp == 0 && tig == 0 && r < hvalid)
           p.lse[t * H + h0 + r] = live ? (m2 + log2f(l2)) * kLn2 : -INFINITY;
       }
       __syncthreads();
+      constexpr int kOChunks = kDv / 8;   // 16-byte chunks per output row
       uint4* outp = reinterpret_cast<uint4*>(static_cast<char*>(p.out) +
-                                             (t * H + h0) * int64_t(kRowBytes));
-      for (int i = tid; i < hvalid * 64; i += kThreads) {
-        const int r = i >> 6, c = i & 63;
+                                             (t * H + h0) * int64_t(kDv * 2));
+      for (int i = tid; i < hvalid * kOChunks; i += kThreads) {
+        const int r = i / kOChunks, c = i % kOChunks;
         outp[i] = *reinterpret_cast<const uint4*>(&ost[r * kOStride + c * 8]);
       }
     }
@@ -371,42 +514,50 @@ __global__ void __launch_bounds__(kThreads, 2) smallh_fwd_kernel(const FwdParams
   cp_async_wait<0>();   // nothing of ours may land after the CTA exits
 }
 
-// CTAs that fit on the current device at once (2 per SM), looked up once per device.
-cudaError_t resident_ctas(int* out) {
-  static int per_dev[64] = {};
+template <int kDqk, int kDv, bool kFp8 = false>
+constexpr int smem_bytes() {
+  return static_cast<int>(sizeof(Smem<kDqk, kDv, kFp8>)) + 1024;
+}
+
+// CTAs of one instantiation that fit on the current device at once, looked up
+// once per device (index `slot` per (kDqk, kDv, fp8) variant).
+template <int kDqk, int kDv, bool kFp8 = false>
+cudaError_t resident_ctas(int slot, int* out) {
+  static int per_dev[5][64] = {};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (per_dev[dev] == 0) {
-    const int smem = static_cast<int>(sizeof(Smem)) + 1024;
-    auto kern = smallh_fwd_kernel<int32_t, false>;
+  if (per_dev[slot][dev] == 0) {
+    const int smem = smem_bytes<kDqk, kDv, kFp8>();
+    auto kern = smallh_fwd_kernel<int32_t, false, kDqk, kDv, false, kFp8>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
     int per_sm = 0, sms = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem)) !=
-        cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Dims<kDqk, kDv>::kThreads,
+                                                           smem)) != cudaSuccess)
       return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
-    per_dev[dev] = std::max(1, per_sm * sms);
+    per_dev[slot][dev] = std::max(1, per_sm * sms);
   }
-  *out = per_dev[dev];
+  *out = per_dev[slot][dev];
   return cudaSuccess;
 }
 
 // Grid: (token CTAs, head groups, splits).  Without splits the CTAs are
 // persistent, each walking tokens blockIdx.x, +gridDim.x, ...; with splits
 // (small T) one CTA per (token, group, split).
-cudaError_t grid_of(int64_t T, int32_t H, int32_t splits, dim3* grid) {
+template <int kDqk, int kDv, bool kFp8 = false>
+cudaError_t grid_of(int slot, int64_t T, int32_t H, int32_t splits, dim3* grid) {
   const int groups = (H + kHG - 1) / kHG;
   int64_t x = T;
   if (splits == 1) {
     int resident = 0;
-    const cudaError_t e = resident_ctas(&resident);
+    const cudaError_t e = resident_ctas<kDqk, kDv, kFp8>(slot, &resident);
     if (e != cudaSuccess) return e;
     x = std::min<int64_t>(T, std::max(1, resident / groups));
   }
@@ -415,39 +566,81 @@ cudaError_t grid_of(int64_t T, int32_t H, int32_t splits, dim3* grid) {
   return cudaSuccess;
 }
 
-template <typename IdxT, bool kSplit>
-cudaError_t launch_typed(const FwdParams& p, cudaStream_t stream) {
-  auto kern = smallh_fwd_kernel<IdxT, kSplit>;
-  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+template <typename IdxT, bool kSplit, int kDqk, int kDv, bool kTrace, bool kFp8 = false>
+cudaError_t launch_typed(int slot, const FwdParams& p, cudaStream_t stream) {
+  auto kern = smallh_fwd_kernel<IdxT, kSplit, kDqk, kDv, kTrace, kFp8>;
+  const int smem = smem_bytes<kDqk, kDv, kFp8>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid;
-  if ((e = grid_of(p.T, p.H, p.splits, &grid)) != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(p);
+  if ((e = grid_of<kDqk, kDv, kFp8>(slot, p.T, p.H, p.splits, &grid)) != cudaSuccess) return e;
+  kern<<<grid, Dims<kDqk, kDv>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int kDqk, int kDv, bool kTrace>
+cudaError_t launch_dims(int slot, const FwdParams& p, cudaStream_t s) {
+  const bool split = p.splits > 1;
+  if (p.idx64)
+    return split ? launch_typed<int64_t, true, kDqk, kDv, kTrace>(slot, p, s)
+                 : launch_typed<int64_t, false, kDqk, kDv, kTrace>(slot, p, s);
+  return split ? launch_typed<int32_t, true, kDqk, kDv, kTrace>(slot, p, s)
+               : launch_typed<int32_t, false, kDqk, kDv, kTrace>(slot, p, s);
+}
+
+template <int kDqk, int kDv, bool kFp8 = false>
+cudaError_t geometry_dims(int slot, int64_t T, int32_t H, int32_t splits, LaunchGeom* g) {
+  dim3 grid;
+  const cudaError_t e = grid_of<kDqk, kDv, kFp8>(slot, T, H, splits, &grid);
+  if (e != cudaSuccess) return e;
+  g->grid_ctas = static_cast<int>(grid.x * grid.y * grid.z);
+  g->threads = Dims<kDqk, kDv>::kThreads;
+  g->cluster = 1;
+  g->smem = smem_bytes<kDqk, kDv, kFp8>();
+  return cudaSuccess;
 }
 
 }  // namespace
 
-int smallh_geometry(int64_t T, int32_t H, int32_t splits, LaunchGeom* g) {
-  dim3 grid;
-  const cudaError_t e = grid_of(T, H, splits, &grid);
-  if (e != cudaSuccess) return static_cast<int>(e);
-  g->grid_ctas = static_cast<int>(grid.x * grid.y * grid.z);
-  g->threads = kThreads;
-  g->cluster = 1;
-  g->smem = static_cast<int>(sizeof(Smem)) + 1024;
-  return 0;
+bool smallh_dims_supported(int32_t d_qk, int32_t d_v) {
+  return (d_qk == 512 && d_v == 512) || (d_qk == 128 && d_v == 128) ||
+         (d_qk == 576 && d_v == 576) || (d_qk == 576 && d_v == 512);
+}
+
+int smallh_geometry(int64_t T, int32_t H, int32_t splits, int32_t d_qk, int32_t d_v,
+                    LaunchGeom* g, bool fp8) {
+  cudaError_t e;
+  if (fp8) return static_cast<int>(geometry_dims<512, 512, true>(4, T, H, splits, g));
+  if (d_qk == 512 && d_v == 512) e = geometry_dims<512, 512>(0, T, H, splits, g);
+  else if (d_qk == 128 && d_v == 128) e = geometry_dims<128, 128>(1, T, H, splits, g);
+  else if (d_qk == 576 && d_v == 576) e = geometry_dims<576, 576>(2, T, H, splits, g);
+  else if (d_qk == 576 && d_v == 512) e = geometry_dims<576, 512>(3, T, H, splits, g);
+  else e = cudaErrorInvalidValue;
+  return static_cast<int>(e);
 }
 
 int launch_smallh(const FwdParams& p, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool split = p.splits > 1;
   cudaError_t e;
-  if (p.idx64)
-    e = split ? launch_typed<int64_t, true>(p, s) : launch_typed<int64_t, false>(p, s);
-  else
-    e = split ? launch_typed<int32_t, true>(p, s) : launch_typed<int32_t, false>(p, s);
+  if (p.kv_fp8) {   // the fp8 cache: 512-wide rows, no read trace
+    if (p.d_qk != 512 || p.d_v != 512 || p.trace != nullptr) return cudaErrorInvalidValue;
+    const bool split = p.splits > 1;
+    if (p.idx64)
+      e = split ? launch_typed<int64_t, true, 512, 512, false, true>(4, p, s)
+                : launch_typed<int64_t, false, 512, 512, false, true>(4, p, s);
+    else
+      e = split ? launch_typed<int32_t, true, 512, 512, false, true>(4, p, s)
+                : launch_typed<int32_t, false, 512, 512, false, true>(4, p, s);
+    return static_cast<int>(e);
+  }
+  // the read trace is built for the 512-wide op only (sparse_mla_fwd_ex)
+  if (p.d_qk == 512 && p.d_v == 512)
+    e = p.trace != nullptr ? launch_dims<512, 512, true>(0, p, s) : launch_dims<512, 512, false>(0, p, s);
+  else if (p.trace != nullptr) e = cudaErrorInvalidValue;
+  else if (p.d_qk == 128 && p.d_v == 128) e = launch_dims<128, 128, false>(1, p, s);
+  else if (p.d_qk == 576 && p.d_v == 576) e = launch_dims<576, 576, false>(2, p, s);
+  else if (p.d_qk == 576 && p.d_v == 512) e = launch_dims<576, 512, false>(3, p, s);
+  else e = cudaErrorInvalidValue;
   return static_cast<int>(e);
 }
 

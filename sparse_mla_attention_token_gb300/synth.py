@@ -220,6 +220,27 @@ def make_inputs(cfg: Config) -> dict:
             "scale": cfg.scale}
 
 
+def fp8_cache(kv_bits: np.ndarray):
+    """An fp8 KV cache of the given bf16 rows, as a cache writer would store it:
+    per row and 128-column block, scale = amax / 448 (1 for an all-zero block)
+    and e4m3fn codes of value / scale, rounded to nearest even (torch's
+    float8_e4m3fn cast).  Returns (uint8 ``[n, 512]``, float32 ``[n, 4]``)."""
+    import torch
+    v = bf16_bits_to_f32(kv_bits).reshape(kv_bits.shape[0], -1, 128)
+    amax = np.abs(v).max(axis=2)
+    scales = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    x = torch.from_numpy(np.ascontiguousarray(v / scales[:, :, None], dtype=np.float32))
+    codes = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return codes.reshape(kv_bits.shape[0], -1), scales
+
+
+def make_dout(cfg: Config, seed: Optional[int] = None) -> np.ndarray:
+    """An output gradient for the backward: bf16 bits ``[T, H, 512]`` of N(0,1)
+    draws from its own seeded stream (seed defaults to the config's + 7919)."""
+    rng = np.random.Generator(np.random.PCG64(cfg.seed + 7919 if seed is None else seed))
+    return _normal_bf16(rng, (cfg.T, cfg.H, D))
+
+
 # ---------------------------------------------------------------- test variants
 def shuffle_rows(idx: np.ndarray, seed: int) -> np.ndarray:
     """Permute every token's slot list independently (seeded)."""

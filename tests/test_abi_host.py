@@ -89,9 +89,10 @@ def test_plan(L):
     # many CTAs: no split; small-head family for H <= 64
     assert binding.sparse_mla_plan(4096, 8, 640) == (0, 1, 1)
     assert binding.sparse_mla_plan(16384, 16, 640) == (0, 1, 1)
-    # few tokens: split over topk, plus the combine launch
-    fam, sp, ln = binding.sparse_mla_plan(4, 16, 640)
-    assert fam == 0 and sp > 1 and ln == 2
+    # few tokens: split over topk (about 128 slots per split), plus the combine launch
+    assert binding.sparse_mla_plan(4, 16, 640) == (0, 5, 2)
+    assert binding.sparse_mla_plan(8, 128, 512) == (0, 4, 2)
+    assert binding.sparse_mla_plan(16, 128, 512) == (1, 1, 1)   # the grid would exceed 2 x SMs
     # forced splits are honoured; topk beyond one CTA's list forces splits
     assert binding.sparse_mla_plan(4096, 16, 640, 4) == (0, 4, 2)
     assert binding.sparse_mla_plan(4096, 16, 5000)[1] >= 3

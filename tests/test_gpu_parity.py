@@ -308,10 +308,12 @@ def test_h128_uses_tcgen05_kernel(B):
 
 @pytest.mark.parametrize("T", [1, 2, 75, 77, 153, 1000])
 def test_h128_token_counts(B, T):
-    # fewer tokens than clusters, one per cluster, several per persistent cluster
+    # fewer tokens than clusters, one per cluster, several per persistent cluster;
+    # one split forces the tcgen05 kernel even where the library would split a
+    # decode-sized call
     cfg = synth.CONFIGS["h128"].with_(T=T, pool=max(8, T // 4), seed=40 + T)
     x = synth.make_inputs(cfg)
-    out, lse, _ = _run(B, x)
+    out, lse, _ = _run(B, x, splits=1)
     O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
     compare(out, lse, O, L)
 
@@ -399,3 +401,38 @@ def test_h128_vs_split_path(B):
     fin = torch.isfinite(l1)
     assert torch.equal(fin, torch.isfinite(l2))
     assert (l1[fin] - l2[fin]).abs().max().item() <= 5e-3
+
+
+# ------------------------------------------------------------ decode-sized calls
+@pytest.mark.parametrize("H", [8, 16, 128])
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16])
+def test_decode_sized_calls(B, H, T):
+    # the last T tokens of an 8192-token context, with the library's split choice
+    # (the split-TOPK path for these sizes, the tcgen05 kernel for H=128 at T=16)
+    cfg = synth.CONFIGS[f"decode_h{H}_t{T}"]
+    x = synth.make_inputs(cfg)
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
+def test_decode_plan():
+    from sparse_mla_attention_token_gb300 import binding
+    for H, want in ((8, 5), (16, 5), (128, 4)):
+        for T in (1, 4, 8):
+            cfg = synth.CONFIGS[f"decode_h{H}_t{T}"]
+            assert binding.sparse_mla_plan(cfg.T, cfg.H, cfg.topk) == (0, want, 2)
+    cfg = synth.CONFIGS["decode_h128_t16"]
+    assert binding.sparse_mla_plan(cfg.T, cfg.H, cfg.topk) == (1, 1, 1)
+
+
+def test_glm_shaped_call_sampled(B):
+    # 16K tokens, 16 heads, top-k 2048, the sequence 2 GiB into a shared pool whose
+    # other rows are NaN: sampled tokens against the oracle, no NaN anywhere
+    cfg = synth.CONFIGS["glm_k2048"]
+    x = synth.make_inputs(cfg)
+    out, lse, _ = _run(B, x)
+    toks = _sample_tokens(cfg.T, n=96)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"], tokens=toks)
+    compare(out, lse, O, L, tokens=toks)
+    assert not torch.isnan(out).any()
