@@ -20,7 +20,8 @@
 //   6. dsink[h] = -sum_t exp(sink[h] - lse[t,h]) delta[t,h]    (bwd_dsink_kernel)
 //
 // Every contraction uses warp-level mma.sync m16n8k16 (bf16 in, fp32 out).
-// dq, dkv and dsink are fp32.  The order in which a row's entries are summed
+// dq, dkv and dsink are fp32; the per-slot interm rows are bf16 (as the page's
+// T * topk * 512 bf16 intermediate) and are summed in fp32 by the gather.  The order in which a row's entries are summed
 // in step 5 follows the fill order of step 4 (atomic), so dkv can differ in
 // its last bits between calls; everything else is deterministic.
 #include <cuda_runtime.h>
@@ -74,8 +75,7 @@ struct __align__(128) DqSmem {
   static constexpr int kRedStride = kBN + 8;   // floats per row of a warp's partials
   static constexpr int kDsStride = kBN + 8;    // bf16 per row of dS' (bank spread for ldmatrix)
   __nv_bfloat16 kv[2][kBN * kHeadDim];         // 2 stages; 16 B chunk c of row r at c ^ (r & 7)
-  float sred[kWarps][kHG * kRedStride];        // per-warp partial S
-  float dpred[kWarps][kHG * kRedStride];       // per-warp partial dP
+  float red[kWarps][kHG * kRedStride];         // per-warp partials: S, then dP
   __nv_bfloat16 ds[kHG * kDsStride];           // dS' of the tile: A operand of dq += dS'.K
   __nv_bfloat16 pt[kHG * kDsStride];           // P of the tile (staged for its global store)
   float lse2[kHG];                             // lse * log2(e) per head (+inf for pad rows)
@@ -84,8 +84,10 @@ struct __align__(128) DqSmem {
   int warp_cnt[kWarps];
 };
 
+// Two CTAs per SM (at most 128 registers, ~97 KB of shared memory each), so
+// that one CTA's barriers overlap the other's contractions.
 template <typename IdxT>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>(smem_raw);
   constexpr int kRS = DqSmem::kRedStride, kDS = DqSmem::kDsStride;
@@ -204,28 +206,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
         mma_16816(dp[nt], da[2 * kp + 1], b2, b3);
       }
     }
+    // the 8 partials of S, then of dP, through one reduction buffer
+    float a[2], b[2];
     {
-      float* sw = sm.sred[warp];
-      float* dw = sm.dpred[warp];
+      float* rw = sm.red[warp];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const int c0 = nt * 8 + 2 * tig;
-        *reinterpret_cast<float2*>(&sw[g * kRS + c0]) = make_float2(s[nt][0], s[nt][1]);
-        *reinterpret_cast<float2*>(&sw[(g + 8) * kRS + c0]) = make_float2(s[nt][2], s[nt][3]);
-        *reinterpret_cast<float2*>(&dw[g * kRS + c0]) = make_float2(dp[nt][0], dp[nt][1]);
-        *reinterpret_cast<float2*>(&dw[(g + 8) * kRS + c0]) = make_float2(dp[nt][2], dp[nt][3]);
+        *reinterpret_cast<float2*>(&rw[g * kRS + c0]) = make_float2(s[nt][0], s[nt][1]);
+        *reinterpret_cast<float2*>(&rw[(g + 8) * kRS + c0]) = make_float2(s[nt][2], s[nt][3]);
       }
-    }
-    __syncthreads();
-    // sum the 8 partials; P = 2^(S sl2 - lse2), dS' = scale P (dP - delta)
-    {
-      float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f};
+      __syncthreads();
+      a[0] = a[1] = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float2 u = *reinterpret_cast<const float2*>(&sm.sred[w][srow * kRS + sc0]);
-        const float2 v = *reinterpret_cast<const float2*>(&sm.dpred[w][srow * kRS + sc0]);
-        a[0] += u.x; a[1] += u.y; b[0] += v.x; b[1] += v.y;
+        const float2 u = *reinterpret_cast<const float2*>(&sm.red[w][srow * kRS + sc0]);
+        a[0] += u.x; a[1] += u.y;
       }
+      __syncthreads();
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int c0 = nt * 8 + 2 * tig;
+        *reinterpret_cast<float2*>(&rw[g * kRS + c0]) = make_float2(dp[nt][0], dp[nt][1]);
+        *reinterpret_cast<float2*>(&rw[(g + 8) * kRS + c0]) = make_float2(dp[nt][2], dp[nt][3]);
+      }
+      __syncthreads();
+      b[0] = b[1] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float2 v = *reinterpret_cast<const float2*>(&sm.red[w][srow * kRS + sc0]);
+        b[0] += v.x; b[1] += v.y;
+      }
+    }
+    // P = 2^(S sl2 - lse2), dS' = scale P (dP - delta)
+    {
       const float l2 = sm.lse2[srow], dl = sm.delta[srow];
       float pr[2], dsv[2];
 #pragma unroll
@@ -313,8 +327,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_interm_kernel(const BwdParams
   constexpr int kK = Sm::kK, kBS = Sm::kBStride, kAS = Sm::kAStride;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tig = lane & 3;
-  const int64_t t = blockIdx.x;
-  const int col0 = blockIdx.y * kIChunk;
+  // blockIdx.x = token * 4 + chunk: a token's four column chunks run together,
+  // so its [P | dS'] rows are read from L2 by three of them
+  const int64_t t = blockIdx.x / (kHeadDim / kIChunk);
+  const int col0 = static_cast<int>(blockIdx.x % (kHeadDim / kIChunk)) * kIChunk;
   const int nv = p.ncnt[t];
   if (nv == 0) return;
 
@@ -331,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_interm_kernel(const BwdParams
     cp_async_commit();
   }
   const __nv_bfloat16* pds = static_cast<const __nv_bfloat16*>(p.pds) + t * p.topk * int64_t(kK);
-  float* interm = p.interm + t * p.topk * int64_t(kHeadDim) + col0 + warp * 16;
+  __nv_bfloat16* interm =
+      static_cast<__nv_bfloat16*>(p.interm) + t * p.topk * int64_t(kHeadDim) + col0 + warp * 16;
   constexpr int kAChunks = kK / 8;   // 16-byte chunks per A row
   for (int m0 = 0; m0 < nv; m0 += kIM) {
     __syncthreads();   // the previous tile's A is no longer read
@@ -374,11 +391,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_interm_kernel(const BwdParams
       for (int half = 0; half < 2; ++half) {
         const int k = m0 + mi * 16 + g + half * 8;
         if (k >= nv) continue;
-        float* dst = interm + int64_t(k) * kHeadDim + 2 * tig;
+        __nv_bfloat16* dst = interm + int64_t(k) * kHeadDim + 2 * tig;
 #pragma unroll
         for (int n = 0; n < 2; ++n)
-          *reinterpret_cast<float2*>(dst + n * 8) =
-              make_float2(acc[mi][n][2 * half], acc[mi][n][2 * half + 1]);
+          *reinterpret_cast<uint32_t*>(dst + n * 8) =
+              pack_bf16x2(acc[mi][n][2 * half], acc[mi][n][2 * half + 1]);
       }
     }
   }
@@ -478,27 +495,25 @@ __global__ void bwd_csr_fill_kernel(const BwdParams p) {
 }
 
 // ------------------------------------------------------------------ 5. dkv gather
-// One CTA of 128 threads per kv row: 4 columns each, fp32 sums of the row's
-// interm entries in list order.
+// One CTA of 128 threads per kv row: 4 columns each (one 8-byte load of bf16
+// per entry), fp32 sums of the row's interm entries in list order.
 __global__ void __launch_bounds__(128) bwd_gather_kernel(const BwdParams p) {
   const int64_t r = blockIdx.x;
   const int b = p.row_cnt[r], e_end = p.row_cnt[r + 1];
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* src = reinterpret_cast<const float4*>(p.interm) + threadIdx.x;
+  const uint2* src = reinterpret_cast<const uint2*>(p.interm) + threadIdx.x;
+  auto add = [&](uint2 v) {
+    acc.x += bf16_lo(v.x); acc.y += bf16_hi(v.x); acc.z += bf16_lo(v.y); acc.w += bf16_hi(v.y);
+  };
   int i = b;
-  for (; i + 4 <= e_end; i += 4) {
-    float4 v[4];
+  for (; i + 8 <= e_end; i += 8) {
+    uint2 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = src[int64_t(p.list[i + u]) * (kHeadDim / 4)];
+    for (int u = 0; u < 8; ++u) v[u] = src[int64_t(p.list[i + u]) * (kHeadDim / 4)];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
-    }
+    for (int u = 0; u < 8; ++u) add(v[u]);
   }
-  for (; i < e_end; ++i) {
-    const float4 v = src[int64_t(p.list[i]) * (kHeadDim / 4)];
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-  }
+  for (; i < e_end; ++i) add(src[int64_t(p.list[i]) * (kHeadDim / 4)]);
   reinterpret_cast<float4*>(p.dkv + r * kHeadDim)[threadIdx.x] = acc;
 }
 
@@ -541,7 +556,7 @@ cudaError_t launch_interm(const BwdParams& p, cudaStream_t s) {
   const int smem = static_cast<int>(sizeof(IntermSmem<kH>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(p.T), kHeadDim / kIChunk);
+  const dim3 grid(static_cast<unsigned>(p.T * (kHeadDim / kIChunk)));
   kern<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
@@ -557,7 +572,7 @@ BwdWorkspace bwd_workspace_layout(int64_t T, int32_t H, int32_t topk, int64_t nu
   w.pds = o;     o += up(e * 2 * H * 2);
   w.crow = o;    o += up(e * 4);
   w.ncnt = o;    o += up(uint64_t(T) * 4);
-  w.interm = o;  o += up(e * kHeadDim * 4);
+  w.interm = o;  o += up(e * kHeadDim * 2);
   w.row_cnt = o; o += up((uint64_t(num_kv) + 1) * 4);
   w.row_cur = o; o += up(uint64_t(num_kv) * 4);
   w.blk = o;     o += up((uint64_t(num_kv) + 1 + kScanBlock) / kScanBlock * 4 + 4);
@@ -574,7 +589,7 @@ int launch_bwd(BwdParams p, void* workspace, void* stream) {
   p.pds = ws + w.pds;
   p.crow = reinterpret_cast<int*>(ws + w.crow);
   p.ncnt = reinterpret_cast<int*>(ws + w.ncnt);
-  p.interm = reinterpret_cast<float*>(ws + w.interm);
+  p.interm = ws + w.interm;
   p.row_cnt = reinterpret_cast<int*>(ws + w.row_cnt);
   p.row_cur = reinterpret_cast<int*>(ws + w.row_cur);
   p.blk = reinterpret_cast<int*>(ws + w.blk);

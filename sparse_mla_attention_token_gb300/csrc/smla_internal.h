@@ -96,7 +96,7 @@ struct BwdParams {
   void* pds;              // [T, topk, 2H] bf16: P, then scale * dS, per compacted slot
   int* crow;              // [T, topk] kv row of each compacted slot
   int* ncnt;              // [T] valid slots per token
-  float* interm;          // [T, topk, 512] fp32: each compacted slot's dkv contribution
+  void* interm;           // [T, topk, 512] bf16: each compacted slot's dkv contribution
   int* row_cnt;           // [num_kv + 1] counts, then exclusive starts (last = total)
   int* row_cur;           // [num_kv] fill cursors
   int* blk;               // scan block totals

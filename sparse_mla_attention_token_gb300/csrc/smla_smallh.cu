@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
       const char* sb = reinterpret_cast<const char*>(p.kv_scale);
 #pragma unroll 4
       for (int i = tid; i < kBN * 33; i += kThreads) {
-        const int r = i / 33, c = i % 33;
+        const int r = static_cast<int>(unsigned(i) / 33u), c = static_cast<int>(unsigned(i) % 33u);
         const int slot = tile * kBN + r;
         const bool ok = slot < nvalid;
         const int64_t row = ok ? rows[slot] : 0;
@@ -236,7 +236,8 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
     constexpr int kChunks = kRowBytes / 16;   // 16-byte chunks per gathered row
 #pragma unroll 4
     for (int i = tid; i < kBN * kChunks; i += kThreads) {
-      const int r = i / kChunks, c = i % kChunks;
+      // non-negative: unsigned division (a shift and a mask for 64 chunks a row)
+      const int r = static_cast<int>(unsigned(i) / kChunks), c = static_cast<int>(unsigned(i) % kChunks);
       const int slot = tile * kBN + r;
       const bool ok = slot < nvalid;
       const char* src = ok ? kvb + int64_t(rows[slot]) * kRowBytes + c * 16 : kvb;
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
       uint4* outp = reinterpret_cast<uint4*>(static_cast<char*>(p.out) +
                                              (t * H + h0) * int64_t(kDv * 2));
       for (int i = tid; i < hvalid * kOChunks; i += kThreads) {
-        const int r = i / kOChunks, c = i % kOChunks;
+        const int r = static_cast<int>(unsigned(i) / kOChunks), c = static_cast<int>(unsigned(i) % kOChunks);
         outp[i] = *reinterpret_cast<const uint4*>(&ost[r * kOStride + c * 8]);
       }
     }
