@@ -21,7 +21,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libsparse_mla.so")
 
 SOURCES = ["api.cpp", "smla_smallh.cu", "smla_h128.cu", "smla_combine.cu", "smla_noalloc.cu",
-           "smla_bwd.cu"]
+           "smla_bwd.cu", "smla_bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I", INCLUDE, "-I", CSRC]

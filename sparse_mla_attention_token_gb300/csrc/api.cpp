@@ -587,20 +587,24 @@ smla_status_t sparse_mla_selftest_wait_timeout(void* stream) {
 smla_status_t sparse_mla_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned int* word = nullptr;
-  const int ge = smla::h128_error_word(&word);
-  if (ge != 0) return cuda_fail(static_cast<cudaError_t>(ge), "cudaGetSymbolAddress(error word)");
-  if (word == nullptr) return SMLA_OK;
-  unsigned int v = 0;
-  e = cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
-  if (v != 0) {
-    const unsigned int zero = 0;
-    e = cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
-    return SMLA_ERR_DEVICE_TIMEOUT;
+  // the forward's and the backward's error words (bounded waits of their tcgen05 kernels)
+  bool expired = false;
+  for (int w = 0; w < 2; ++w) {
+    unsigned int* word = nullptr;
+    const int ge = w == 0 ? smla::h128_error_word(&word) : smla::bwd_error_word(&word);
+    if (ge != 0) return cuda_fail(static_cast<cudaError_t>(ge), "cudaGetSymbolAddress(error word)");
+    if (word == nullptr) continue;
+    unsigned int v = 0;
+    e = cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (v != 0) {
+      const unsigned int zero = 0;
+      e = cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+      expired = true;
+    }
   }
-  return SMLA_OK;
+  return expired ? SMLA_ERR_DEVICE_TIMEOUT : SMLA_OK;
 }
 
 const char* sparse_mla_strerror(int32_t status) {

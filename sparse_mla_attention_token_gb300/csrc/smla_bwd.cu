@@ -12,7 +12,8 @@
 //      score gradient dS' = scale P (dP - delta), dq += dS'.K; P and dS' are
 //      written out per compacted slot for step 3              (bwd_dq_kernel)
 //   3. the per-(token, slot) row "interm" = P^T dO + dS'^T Q, a contraction
-//      over the heads                                          (bwd_interm_kernel)
+//      over the heads (bwd_interm_kernel; at H = 128 the tcgen05 kernel of
+//      smla_bwd_tc.cu)
 //   4. an inverted index: the (token, slot) entries of every kv row
 //      (histogram, exclusive scan, fill)                       (bwd_csr_*)
 //   5. dkv[r] = sum of the interm rows of r's entries: a gather, no atomics
@@ -601,11 +602,11 @@ int launch_bwd(BwdParams p, void* workspace, void* stream) {
   e = p.idx64 ? launch_dq<int64_t>(p, s) : launch_dq<int32_t>(p, s);
   if (e != cudaSuccess) return e;
   switch (p.H) {
+    case 128: e = static_cast<cudaError_t>(launch_bwd_interm_tc(p, s)); break;   // tcgen05
     case 8: e = launch_interm<8>(p, s); break;
     case 16: e = launch_interm<16>(p, s); break;
     case 32: e = launch_interm<32>(p, s); break;
     case 64: e = launch_interm<64>(p, s); break;
-    case 128: e = launch_interm<128>(p, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;

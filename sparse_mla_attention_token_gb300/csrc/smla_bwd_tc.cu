@@ -1,0 +1,243 @@
+// tcgen05 form of the backward's per-slot dkv contraction, H = 128 ("Sparse
+// MLA training backward", aiter PR #4766, section "Structure": the dKV-interm
+// step, a contraction over all heads of the gathered slots' P and dS).
+//
+//   interm[t, k, d] = sum_c A[t, k, c] * B[t, c, d],   c < 2H = 256
+//   A[t, k, :] = [P(t, :, k) | scale * dS(t, :, k)]    (the workspace rows the
+//                                                       dq kernel writes, bf16)
+//   B[t, c, :] = dO[t, c, :] for c < H, q[t, c - H, :] for c >= H
+//
+// One CTA per (token, 128-slot tile, 256-column half of D): M = 128 slots,
+// N = 256, K = 256 in four 64-wide chunks.  Warp 0 lane 0 loads each chunk with
+// 2-D TMA (A: one 128 x 64 box of the [T * topk, 256] workspace; B: four 64 x
+// 64 boxes of dO or q, the MN-major operand) into a two-stage ring; warp 1
+// lane 0 owns the 256 TMEM columns and issues four M128 N256 K16 MMAs per
+// chunk; all four warps then read the accumulator (thread = TMEM lane = slot)
+// and store the tile's valid rows as bf16.  96 KB of shared memory and 256
+// TMEM columns: two CTAs per SM, one's epilogue under the other's MMAs.
+//
+// Every wait is bounded (~2 s): on expiry the CTA records an error in the
+// backward's error word (read by sparse_mla_device_status), waits for what it
+// issued, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "smla_device.cuh"
+#include "smla_internal.h"
+#include "smla_sm100.cuh"
+
+namespace smla {
+
+__device__ unsigned int g_bwd_error;
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreadsTc = 128;
+constexpr int kM = 128;                          // slots per tile
+constexpr int kNh = 256;                         // output columns per CTA
+constexpr int kKc = 64;                          // contraction chunk
+constexpr int kH = 128;
+constexpr int kChunks = 2 * kH / kKc;            // 4
+constexpr int kStagesTc = 2;
+constexpr uint32_t kABytes = kM * kKc * 2;       // 16 KB: [128 rows][128 B]
+constexpr uint32_t kBBytes = kKc * kNh * 2;      // 32 KB: [4 column blocks][64 K rows][128 B]
+constexpr uint32_t kStageBytesTc = kABytes + kBBytes;
+constexpr uint32_t kBarOffTc = kStagesTc * kStageBytesTc;
+constexpr uint32_t kSmemTc = kBarOffTc + 128 + 1024;   // barriers + alignment slack
+constexpr long long kTimeoutTc = 4000000000LL;         // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t bar_addr_tc(const uint64_t& b) { return smem_u32(&b); }
+
+struct TcBars {
+  uint64_t full[kStagesTc], empty[kStagesTc], done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_tc(uint32_t bar, uint32_t parity, TcBars* b, bool drain) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15) == 0) {
+      if (!drain && *reinterpret_cast<volatile int*>(&b->abort_flag)) return false;
+      if (clock64() - t0 > kTimeoutTc) {
+        *reinterpret_cast<volatile int*>(&b->abort_flag) = 1;
+        atomicOr(&g_bwd_error, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 2)
+    bwd_interm_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_q, const BwdParams p, int ntile) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  TcBars* b = reinterpret_cast<TcBars*>(base + kBarOffTc);
+  const uint32_t sbase = smem_u32(base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dh = blockIdx.x & 1;
+  const int64_t unit = blockIdx.x >> 1;
+  const int64_t t = unit / ntile;
+  const int tile = static_cast<int>(unit % ntile);
+  const int nv = p.ncnt[t];
+  if (tile * kM >= nv) return;   // uniform: this tile holds no valid slot
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesTc; ++s) {
+      mbar_init(bar_addr_tc(b->full[s]), 1);
+      mbar_init(bar_addr_tc(b->empty[s]), 1);
+    }
+    mbar_init(bar_addr_tc(b->done), 1);
+    mbar_init(bar_addr_tc(b->drain), 1);
+    b->abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&b->tmem_base), kNh);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b->tmem_base;
+  const int row0 = static_cast<int>(t * p.topk + int64_t(tile) * kM);   // < 2^31 (host check)
+  const int qrow0 = static_cast<int>(t * kH);
+
+  if (warp == 0 && lane == 0) {
+    // producer: chunk c = heads 64c..64c+63 of [P | dS'] against rows of dO (c < 2) or q
+    uint32_t loaded = 0;
+    for (int c = 0; c < kChunks; ++c) {
+      const int s = c % kStagesTc;
+      if (c >= kStagesTc && !wait_tc(bar_addr_tc(b->empty[s]), ((c / kStagesTc) - 1) & 1, b, false))
+        break;
+      const uint32_t st = sbase + s * kStageBytesTc;
+      mbar_arrive_expect_tx(bar_addr_tc(b->full[s]), kStageBytesTc);
+      tma_load_2d(st, &tm_a, kKc * c, row0, bar_addr_tc(b->full[s]));
+      const CUtensorMap* mb = c < 2 ? &tm_do : &tm_q;
+      const int brow = qrow0 + kKc * (c & 1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tma_load_2d(st + kABytes + j * 8192, mb, kNh * dh + 64 * j, brow, bar_addr_tc(b->full[s]));
+      ++loaded;
+    }
+    // drain: every load issued has landed before the CTA may exit
+    for (uint32_t c = loaded >= kStagesTc ? loaded - kStagesTc : 0; c < loaded; ++c)
+      wait_tc(bar_addr_tc(b->full[c % kStagesTc]), (c / kStagesTc) & 1, b, true);
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kM, kNh, false, true);
+    bool ok = true;
+    for (int c = 0; c < kChunks && ok; ++c) {
+      const int s = c % kStagesTc;
+      if (!(ok = wait_tc(bar_addr_tc(b->full[s]), (c / kStagesTc) & 1, b, false))) break;
+      tc_fence_after();
+      const uint32_t st = sbase + s * kStageBytesTc;
+#pragma unroll
+      for (int kk = 0; kk < kKc / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(st + kk * 32, 16, 1024);                 // K-major A
+        const uint64_t bd = sdesc_sw128(st + kABytes + kk * 16 * 128, 8192, 1024);  // MN-major B
+        mma_bf16_ss(tmem, ad, bd, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(bar_addr_tc(b->empty[s]));
+    }
+    mma_commit(bar_addr_tc(ok ? b->done : b->drain));
+    if (!ok) wait_tc(bar_addr_tc(b->drain), 0, b, true);   // MMAs issued so far completed
+  }
+  __syncwarp();
+  // epilogue: thread = TMEM lane = slot of the tile; bf16 rows to the workspace
+  const bool done = __all_sync(0xffffffffu, wait_tc(bar_addr_tc(b->done), 0, b, false));
+  if (done) {
+    tc_fence_after();
+    const int r = 32 * warp + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const bool live = tile * kM + r < nv;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.interm) +
+                         (int64_t(row0) + r) * kHeadDim + kNh * dh;
+#pragma unroll 1
+    for (int cc = 0; cc < kNh / 32; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(tl + 32 * cc, v);
+      tmem_wait_ld();
+      if (live) {
+        uint4* o = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kNh);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tc() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a [rows, cols] row-major matrix, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                 uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_tc();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_bwd_interm_tc(const BwdParams& p, void* stream) {
+  if (p.H != kH || p.T <= 0 || p.topk <= 0) return static_cast<int>(cudaErrorInvalidValue);
+  auto kern = bwd_interm_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemTc));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  CUtensorMap ta, tdo, tq;
+  if (!make_map_2d(&ta, p.pds, uint64_t(p.T) * p.topk, 2 * kH, 64, kM) ||
+      !make_map_2d(&tdo, p.dout, uint64_t(p.T) * kH, kHeadDim, 64, 64) ||
+      !make_map_2d(&tq, p.q, uint64_t(p.T) * kH, kHeadDim, 64, 64))
+    return static_cast<int>(cudaErrorInvalidValue);
+  const int ntile = (p.topk + kM - 1) / kM;
+  const int64_t blocks = p.T * ntile * 2;
+  kern<<<static_cast<unsigned>(blocks), kThreadsTc, kSmemTc, static_cast<cudaStream_t>(stream)>>>(
+      ta, tdo, tq, p, ntile);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int bwd_error_word(unsigned int** addr) {
+  return static_cast<int>(cudaGetSymbolAddress(reinterpret_cast<void**>(addr), g_bwd_error));
+}
+
+}  // namespace smla
