@@ -10,7 +10,8 @@
 //      S = Q.K^T and dP = dO.V^T from one gathered tile (K == V), the exact
 //      probabilities P = exp(scale S - lse) from the saved lse, the scaled
 //      score gradient dS' = scale P (dP - delta), dq += dS'.K; P and dS' are
-//      written out per compacted slot for step 3              (bwd_dq_kernel)
+//      written out per compacted slot for step 3              (bwd_dq_kernel;
+//      at H = 128, dq = dS'.K is the tcgen05 GEMM of smla_bwd_tc.cu)
 //   3. the per-(token, slot) row "interm" = P^T dO + dS'^T Q, a contraction
 //      over the heads (bwd_interm_kernel; at H = 128 the tcgen05 kernel of
 //      smla_bwd_tc.cu)
@@ -71,6 +72,43 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const BwdParams p) {
   if (lane == 0) p.delta[row] = acc;
 }
 
+// ------------------------------------------------------------------ compaction (H = 128)
+// One CTA per token: the valid slots' rows in slot order (full-width check),
+// for the tcgen05 kernels that follow.
+template <typename IdxT>
+__global__ void __launch_bounds__(kThreads) bwd_compact_kernel(const BwdParams p) {
+  __shared__ int warp_cnt[kWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t t = blockIdx.x;
+  const IdxT* idx = static_cast<const IdxT*>(p.idx) + t * p.topk;
+  int* out = p.crow + t * p.topk;
+  int nv = 0;
+  for (int base = 0; base < p.topk; base += kThreads) {
+    const int j = base + tid;
+    bool v = false;
+    int row = -1;
+    if (j < p.topk) {
+      const IdxT x = idx[j];
+      v = slot_valid<IdxT>(x, p.num_kv);
+      if (v) row = static_cast<int>(x);   // exact: num_kv < 2^31
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) warp_cnt[warp] = __popc(ball);
+    __syncthreads();
+    int off = nv, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = warp_cnt[w];
+      off += (w < warp) ? c : 0;
+      total += c;
+    }
+    if (v) out[off + __popc(ball & ((1u << lane) - 1u))] = row;
+    nv += total;
+    __syncthreads();
+  }
+  if (tid == 0) p.ncnt[t] = nv;
+}
+
 // ------------------------------------------------------------------ 2. dq, P, dS'
 struct __align__(128) DqSmem {
   static constexpr int kRedStride = kBN + 8;   // floats per row of a warp's partials
@@ -86,8 +124,10 @@ struct __align__(128) DqSmem {
 };
 
 // Two CTAs per SM (at most 128 registers, ~97 KB of shared memory each), so
-// that one CTA's barriers overlap the other's contractions.
-template <typename IdxT>
+// that one CTA's barriers overlap the other's contractions.  kDq = false (H =
+// 128): only S, dP, P and dS' -- dq then comes from the tcgen05 GEMM of
+// smla_bwd_tc.cu.
+template <typename IdxT, bool kDq>
 __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>(smem_raw);
@@ -270,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
       }
     }
     // dq += dS'.K over this warp's 64 columns
-    {
+    if constexpr (kDq) {
       const uint32_t ds_base = smem_u32(sm.ds);
 #pragma unroll
       for (int ks = 0; ks < kBN / 16; ++ks) {
@@ -292,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
     }
   }
   cp_async_wait<0>();
+  if constexpr (!kDq) return;
   // dq rows of the group (fp32)
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
@@ -540,9 +581,9 @@ __global__ void __launch_bounds__(256) bwd_dsink_kernel(const BwdParams p) {
   }
 }
 
-template <typename IdxT>
+template <typename IdxT, bool kDq>
 cudaError_t launch_dq(const BwdParams& p, cudaStream_t s) {
-  auto kern = bwd_dq_kernel<IdxT>;
+  auto kern = bwd_dq_kernel<IdxT, kDq>;
   const int smem = static_cast<int>(sizeof(DqSmem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -599,7 +640,18 @@ int launch_bwd(BwdParams p, void* workspace, void* stream) {
   const int64_t rows = p.T * p.H;
   bwd_delta_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = p.idx64 ? launch_dq<int64_t>(p, s) : launch_dq<int32_t>(p, s);
+  // at H = 128: compaction, then S / dP / P / dS' and dq = dS'.K as tcgen05 kernels
+  if (p.H == 128) {
+    if (p.idx64)
+      bwd_compact_kernel<int64_t><<<static_cast<unsigned>(p.T), kThreads, 0, s>>>(p);
+    else
+      bwd_compact_kernel<int32_t><<<static_cast<unsigned>(p.T), kThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = static_cast<cudaError_t>(launch_bwd_sdp_tc(p, s));
+    if (e == cudaSuccess) e = static_cast<cudaError_t>(launch_bwd_dq_tc(p, s));
+  } else {
+    e = p.idx64 ? launch_dq<int64_t, true>(p, s) : launch_dq<int32_t, true>(p, s);
+  }
   if (e != cudaSuccess) return e;
   switch (p.H) {
     case 128: e = static_cast<cudaError_t>(launch_bwd_interm_tc(p, s)); break;   // tcgen05

@@ -188,6 +188,334 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   }
 }
 
+// dq = scale * dS . K for H = 128: M = 128 heads, N = 256 (a D half), K = the
+// token's valid slots in 64-slot chunks.  A = (scale dS)^T, MN-major: each
+// slot's 128 dS' values (256 bytes of the workspace row) as two 128-byte rows of
+// two 64-head blocks; B = the gathered kv half rows, MN-major (the forward's
+// stage layout).  Warps 0-3 gather both with 16-byte cp.async into a two-stage
+// ring (slots past the valid count zero-filled, so the uninitialised workspace
+// past them never enters a sum) and then run the epilogue; warp 4 lane 0 owns
+// TMEM and issues four M128 N256 K16 MMAs per chunk.
+constexpr int kDqThreads = 160;
+constexpr int kDqChunk = 64;                         // slots per chunk
+constexpr uint32_t kDqA = kDqChunk * kH * 2;         // 16 KB: [2 head blocks][64 slots][128 B]
+constexpr uint32_t kDqB = kDqChunk * kNh * 2;        // 32 KB: [4 column blocks][64 slots][128 B]
+constexpr uint32_t kDqStage = kDqA + kDqB;
+constexpr uint32_t kDqBarOff = 2 * kDqStage;
+constexpr uint32_t kDqSmem = kDqBarOff + 128 + 1024;
+
+__global__ void __launch_bounds__(kDqThreads, 2)
+    bwd_dq_tc_kernel(const BwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  TcBars* b = reinterpret_cast<TcBars*>(base + kDqBarOff);
+  const uint32_t sbase = smem_u32(base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int dh = blockIdx.x & 1;
+  const int64_t t = blockIdx.x >> 1;
+  const int nv = p.ncnt[t];
+  float* dq = p.dq + (t * kH) * int64_t(kHeadDim) + kNh * dh;
+  if (nv == 0) {   // no valid slot: dq = 0 (uniform)
+    if (tid < kH) {
+      float4* o = reinterpret_cast<float4*>(dq + int64_t(tid) * kHeadDim);
+      for (int i = 0; i < kNh / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_addr_tc(b->full[s]), 128);     // the four gather warps
+      mbar_init(bar_addr_tc(b->empty[s]), 1);
+    }
+    mbar_init(bar_addr_tc(b->done), 1);
+    mbar_init(bar_addr_tc(b->drain), 1);
+    b->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(&b->tmem_base), kNh);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b->tmem_base;
+  const int nchunks = (nv + kDqChunk - 1) / kDqChunk;
+
+  if (warp < 4) {
+    const char* pds = static_cast<const char*>(p.pds) + t * p.topk * int64_t(2 * kH * 2);
+    const int* crow = p.crow + t * p.topk;
+    const char* kvb = static_cast<const char*>(p.kv) + kNh * 2 * dh;   // this CTA's D half
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c & 1;
+      if (c >= 2 &&
+          !(ok = __all_sync(0xffffffffu, wait_tc(bar_addr_tc(b->empty[s]), ((c >> 1) - 1) & 1, b, false))))
+        break;
+      const uint32_t st = sbase + s * kDqStage;
+      // A: slot r's dS' (heads 0-127) = 16 chunks: head block hb = chunk / 8
+      for (int i = tid; i < kDqChunk * 16; i += 128) {
+        const int r = i >> 4, q = i & 15;
+        const int slot = c * kDqChunk + r;
+        const bool v = slot < nv;
+        const char* src = v ? pds + int64_t(slot) * (2 * kH * 2) + kH * 2 + q * 16 : pds;
+        cp_async_16(st + (q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4), src, v ? 16u : 0u);
+      }
+      // B: slot r's kv half row = 32 chunks: column block cb = chunk / 8
+      for (int i = tid; i < kDqChunk * 32; i += 128) {
+        const int r = i >> 5, q = i & 31;
+        const int slot = c * kDqChunk + r;
+        const bool v = slot < nv;
+        const char* src = v ? kvb + int64_t(crow[slot]) * 1024 + q * 16 : kvb;
+        cp_async_16(st + kDqA + (q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4), src,
+                    v ? 16u : 0u);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();   // visible to the tensor core's async proxy
+      mbar_arrive(bar_addr_tc(b->full[s]));
+    }
+    cp_async_wait<0>();
+  } else if (lane == 0) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kH, kNh, true, true);
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c & 1;
+      if (!(ok = wait_tc(bar_addr_tc(b->full[s]), (c >> 1) & 1, b, false))) break;
+      tc_fence_after();
+      const uint32_t st = sbase + s * kDqStage;
+#pragma unroll
+      for (int kk = 0; kk < kDqChunk / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(st + kk * 16 * 128, 8192, 1024);          // MN-major A
+        const uint64_t bd = sdesc_sw128(st + kDqA + kk * 16 * 128, 8192, 1024);   // MN-major B
+        mma_bf16_ss(tmem, ad, bd, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(bar_addr_tc(b->empty[s]));
+    }
+    mma_commit(bar_addr_tc(ok ? b->done : b->drain));
+    if (!ok) wait_tc(bar_addr_tc(b->drain), 0, b, true);
+  }
+  __syncwarp();
+  if (warp < 4) {
+    // epilogue: thread = TMEM lane = head; its 256 dq columns in fp32
+    const bool done = __all_sync(0xffffffffu, wait_tc(bar_addr_tc(b->done), 0, b, false));
+    if (done) {
+      tc_fence_after();
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+      float4* o = reinterpret_cast<float4*>(dq + int64_t(tid) * kHeadDim);
+#pragma unroll 1
+      for (int cc = 0; cc < kNh / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(tl + 32 * cc, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o[8 * cc + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                      __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kNh);
+  }
+}
+
+// S and dP for H = 128, transposed so that the slots are the MMA's M: per
+// (token, 128-slot tile), S^T = K . Q^T and dP^T = K . dO^T (M = 128 slots,
+// N = 128 heads, K = 512 in eight 64-column chunks; both operands K-major).
+// Warps 0-3 gather the tile's kv rows chunk by chunk (16-byte cp.async, 128 B a
+// row, slots past the valid count zero-filled); warp 4 lane 0 loads the Q and
+// dO chunks with 2-D TMA, owns 256 TMEM columns (S^T, then dP^T) and issues
+// eight M128 N128 K16 MMAs a chunk.  The epilogue (thread = TMEM lane = slot)
+// forms P = 2^(S scale log2e - lse log2e) from the saved lse and
+// dS' = scale P (dP - delta), and writes the slot's workspace row [P | dS'].
+constexpr int kSdThreads = 160;
+constexpr int kSdM = 128;                            // slots per tile
+constexpr int kSdChunks = kHeadDim / 64;             // 8
+constexpr uint32_t kSdA = kSdM * 128;                // 16 KB: [128 slots][128 B]
+constexpr uint32_t kSdB = kH * 128;                  // 16 KB: [128 heads][128 B]
+constexpr uint32_t kSdStage = kSdA + 2 * kSdB;       // 48 KB
+constexpr uint32_t kSdBarOff = 2 * kSdStage;
+constexpr uint32_t kSdSmem = kSdBarOff + 128 + 2 * kH * 4 + 1024;
+
+struct SdBars {
+  uint64_t full[2], tma[2], empty[2], done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_sd(uint32_t bar, uint32_t parity, SdBars* b, bool drain) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15) == 0) {
+      if (!drain && *reinterpret_cast<volatile int*>(&b->abort_flag)) return false;
+      if (clock64() - t0 > kTimeoutTc) {
+        *reinterpret_cast<volatile int*>(&b->abort_flag) = 1;
+        atomicOr(&g_bwd_error, 2u);
+        return false;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSdThreads, 2)
+    bwd_sdp_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_do, const BwdParams p, int ntile) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  SdBars* b = reinterpret_cast<SdBars*>(base + kSdBarOff);
+  float* lse2 = reinterpret_cast<float*>(base + kSdBarOff + 128);   // [128] lse * log2 e
+  float* dlt = lse2 + kH;                                           // [128] delta
+  const uint32_t sbase = smem_u32(base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int64_t t = blockIdx.x / ntile;
+  const int tile = static_cast<int>(blockIdx.x % ntile);
+  const int nv = p.ncnt[t];
+  if (tile * kSdM >= nv) return;   // uniform
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_addr_tc(b->full[s]), 128);   // the four gather warps
+      mbar_init(bar_addr_tc(b->tma[s]), 1);      // Q and dO chunks (TMA bytes)
+      mbar_init(bar_addr_tc(b->empty[s]), 1);
+    }
+    mbar_init(bar_addr_tc(b->done), 1);
+    mbar_init(bar_addr_tc(b->drain), 1);
+    b->abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+  }
+  if (tid < kH) {
+    lse2[tid] = p.lse[t * kH + tid] * kLog2e;
+    dlt[tid] = p.delta[t * kH + tid];
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(&b->tmem_base), 2 * kH);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b->tmem_base;
+  const int slot0 = tile * kSdM;
+  const int* crow = p.crow + t * p.topk;
+
+  if (warp < 4) {
+    // gather: thread = slot row r of the tile; 8 chunks of 16 B per 64-column chunk
+    const int r = tid;
+    const bool v = slot0 + r < nv;
+    const char* src_row =
+        static_cast<const char*>(p.kv) + (v ? int64_t(crow[slot0 + r]) * 1024 : 0);
+    bool ok = true;
+    for (int c = 0; c < kSdChunks && ok; ++c) {
+      const int s = c & 1;
+      if (c >= 2 &&
+          !(ok = __all_sync(0xffffffffu, wait_sd(bar_addr_tc(b->empty[s]), ((c >> 1) - 1) & 1, b, false))))
+        break;
+      const uint32_t dst = sbase + s * kSdStage + r * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        cp_async_16(dst + ((q ^ (r & 7)) << 4), src_row + c * 128 + q * 16, v ? 16u : 0u);
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(bar_addr_tc(b->full[s]));
+    }
+    cp_async_wait<0>();
+  } else if (lane == 0) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kSdM, kH, false, false);
+    const int qrow = static_cast<int>(t * kH);
+    bool ok = true;
+    uint32_t loaded = 0;
+    auto load = [&](int c) {
+      const int s = c & 1;
+      const uint32_t st = sbase + s * kSdStage;
+      mbar_arrive_expect_tx(bar_addr_tc(b->tma[s]), 2 * kSdB);
+      tma_load_2d(st + kSdA, &tm_q, 64 * c, qrow, bar_addr_tc(b->tma[s]));
+      tma_load_2d(st + kSdA + kSdB, &tm_do, 64 * c, qrow, bar_addr_tc(b->tma[s]));
+      ++loaded;
+    };
+    load(0);
+    load(1);
+    for (int c = 0; c < kSdChunks && ok; ++c) {
+      const int s = c & 1;
+      if (!(ok = wait_sd(bar_addr_tc(b->full[s]), (c >> 1) & 1, b, false))) break;
+      if (!(ok = wait_sd(bar_addr_tc(b->tma[s]), (c >> 1) & 1, b, false))) break;
+      tc_fence_after();
+      const uint32_t st = sbase + s * kSdStage;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = sdesc_sw128(st + kk * 32, 16, 1024);
+        const uint64_t bq = sdesc_sw128(st + kSdA + kk * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(st + kSdA + kSdB + kk * 32, 16, 1024);
+        const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
+        mma_bf16_ss(tmem, ad, bq, kIdesc, acc);            // S^T
+        mma_bf16_ss(tmem + kH, ad, bd, kIdesc, acc);       // dP^T
+      }
+      mma_commit(bar_addr_tc(b->empty[s]));
+      if (c + 2 < kSdChunks) {
+        // the stage's Q / dO may be replaced once these MMAs have read it
+        if (!(ok = wait_sd(bar_addr_tc(b->empty[s]), (c >> 1) & 1, b, false))) break;
+        load(c + 2);
+      }
+    }
+    mma_commit(bar_addr_tc(ok ? b->done : b->drain));
+    if (!ok) wait_sd(bar_addr_tc(b->drain), 0, b, true);
+    // every TMA load issued has landed
+    for (uint32_t c = loaded >= 2 ? loaded - 2 : 0; c < loaded; ++c)
+      wait_sd(bar_addr_tc(b->tma[c & 1]), (c >> 1) & 1, b, true);
+  }
+  __syncwarp();
+  if (warp < 4) {
+    const bool done = __all_sync(0xffffffffu, wait_sd(bar_addr_tc(b->done), 0, b, false));
+    if (done) {
+      tc_fence_after();
+      const int r = tid;
+      const bool v = slot0 + r < nv;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+      const float sl2 = p.scale * kLog2e;
+      uint4* row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.pds) +
+                                            (t * p.topk + slot0 + r) * int64_t(2 * kH));
+#pragma unroll 1
+      for (int hc = 0; hc < kH / 32; ++hc) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tl + 32 * hc, sv);
+        tmem_ld32(tl + kH + 32 * hc, dv);
+        tmem_wait_ld();
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = 32 * hc + 2 * i;
+          const float p0 = ex2(__uint_as_float(sv[2 * i]) * sl2 - lse2[h]);
+          const float p1 = ex2(__uint_as_float(sv[2 * i + 1]) * sl2 - lse2[h + 1]);
+          pw[i] = pack_bf16x2(p0, p1);
+          dw[i] = pack_bf16x2(p.scale * p0 * (__uint_as_float(dv[2 * i]) - dlt[h]),
+                              p.scale * p1 * (__uint_as_float(dv[2 * i + 1]) - dlt[h + 1]));
+        }
+        if (v) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            row[4 * hc + q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+            row[16 + 4 * hc + q] = make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kH);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_tc() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -233,6 +561,32 @@ int launch_bwd_interm_tc(const BwdParams& p, void* stream) {
   const int64_t blocks = p.T * ntile * 2;
   kern<<<static_cast<unsigned>(blocks), kThreadsTc, kSmemTc, static_cast<cudaStream_t>(stream)>>>(
       ta, tdo, tq, p, ntile);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_bwd_dq_tc(const BwdParams& p, void* stream) {
+  if (p.H != kH || p.T <= 0) return static_cast<int>(cudaErrorInvalidValue);
+  auto kern = bwd_dq_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kDqSmem));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  kern<<<static_cast<unsigned>(p.T * 2), kDqThreads, kDqSmem, static_cast<cudaStream_t>(stream)>>>(p);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_bwd_sdp_tc(const BwdParams& p, void* stream) {
+  if (p.H != kH || p.T <= 0 || p.topk <= 0) return static_cast<int>(cudaErrorInvalidValue);
+  auto kern = bwd_sdp_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSdSmem));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  CUtensorMap tq, tdo;
+  if (!make_map_2d(&tq, p.q, uint64_t(p.T) * kH, kHeadDim, 64, kH) ||
+      !make_map_2d(&tdo, p.dout, uint64_t(p.T) * kH, kHeadDim, 64, kH))
+    return static_cast<int>(cudaErrorInvalidValue);
+  const int ntile = (p.topk + kSdM - 1) / kSdM;
+  kern<<<static_cast<unsigned>(p.T * ntile), kSdThreads, kSdSmem,
+         static_cast<cudaStream_t>(stream)>>>(tq, tdo, p, ntile);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -116,8 +116,11 @@ struct BwdWorkspace {
 BwdWorkspace bwd_workspace_layout(int64_t T, int32_t H, int32_t topk, int64_t num_kv);
 // All backward kernels on `stream`; returns a cudaError_t value.
 int launch_bwd(BwdParams p, void* workspace, void* stream);
-// tcgen05 form of the per-slot dkv contraction (H = 128); workspace pointers set.
+// tcgen05 forms of the per-slot dkv contraction and of dq = dS'.K (H = 128);
+// workspace pointers set, P / dS' and the compacted rows written.
 int launch_bwd_interm_tc(const BwdParams& p, void* stream);
+int launch_bwd_dq_tc(const BwdParams& p, void* stream);
+int launch_bwd_sdp_tc(const BwdParams& p, void* stream);
 // Device address of the backward's error word (bounded waits of its tcgen05 kernel).
 int bwd_error_word(unsigned int** addr);
 
