@@ -578,16 +578,18 @@ def run_ours(args, cfg) -> None:
         pw_sampler = ClockSampler(_physical_gpu(local_rank))
         pw_sampler.start()
         p0 = time.time()
+        if args.per_workload == "all":
+            names = names + ["fp8_small_head", "fp8_sweep_k640", "bwd_h128"]
         for n in names:
             if n == cfg.name:
                 continue
-            pw[n] = measure_workload(n, args, dev, flush, stream, peaks)
-            torch.cuda.empty_cache()
-        if args.per_workload == "all":
-            for n in ("small_head", "sweep_k640"):
-                pw[f"fp8_{n}"] = measure_fp8(n, args, dev, flush, stream, peaks)
-                torch.cuda.empty_cache()
-            pw["bwd_h128"] = measure_backward("h128", args, dev, flush, stream, peaks)
+            # fp8_<config>: the fp8-cache forward; bwd_<config>: the training backward
+            if n.startswith("fp8_"):
+                pw[n] = measure_fp8(n[4:], args, dev, flush, stream, peaks)
+            elif n.startswith("bwd_"):
+                pw[n] = measure_backward(n[4:], args, dev, flush, stream, peaks)
+            else:
+                pw[n] = measure_workload(n, args, dev, flush, stream, peaks)
             torch.cuda.empty_cache()
         pw_sampler.mark(p0, time.time())
         line["per_workload"] = pw
@@ -655,7 +657,8 @@ def main(argv=None) -> int:
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--per-workload", default="all",
-                    help="other workloads to report: all, none, or a comma-separated list")
+                    help="other workloads to report: all, none, or a comma-separated list "
+                         "(fp8_<config>: fp8-cache forward; bwd_<config>: training backward)")
     ap.add_argument("--pw-steps", type=int, default=20,
                     help="timed calls per workload in per_workload")
     ap.add_argument("--reference-budget", type=float, default=120.0,

@@ -71,6 +71,36 @@ def test_fp8_variants(B, variant):
     _run(B, x, kv8, sc)
 
 
+@pytest.mark.parametrize("variant", ["wide_scales", "wide_scales_t4", "big_q", "tiny_q"])
+def test_fp8_value_ranges(B, variant):
+    # the fp16 operands' range handling: Q far outside fp16's range either way (the
+    # softmax scale compensates, so the logits keep their size), and block scales that
+    # differ by up to 2^12 between rows, so that the largest scale changes from tile to tile
+    # (600 tokens: one launch without splits; wide_scales_t4: four tokens, a split launch
+    # and the combine)
+    cfg = synth.CONFIGS["tiny"].with_(T=4 if variant.endswith("t4") else 600, H=16, pool=400,
+                                      ratio=1, topk=300, window=64, seed=430)
+    x = synth.make_inputs(cfg)
+    kv8, sc = synth.fp8_cache(x["kv"])
+    if variant.startswith("wide_scales"):
+        e = np.random.default_rng(431).integers(-6, 7, size=sc.shape)
+        sc = (sc * np.exp2(e)).astype(np.float32)
+    else:
+        k = 20 if variant == "big_q" else -30
+        q = synth.bf16_bits_to_f32(x["q"]) * np.float32(2.0 ** k)
+        x["q"] = synth.bf16_bits(q.astype(np.float32))
+        x["scale"] = float(np.float32(x["scale"] * 2.0 ** -k))
+    q = torch.from_numpy(x["q"].view(np.int16)).view(torch.bfloat16).to(DEV)
+    out, lse = B.sparse_mla_fwd_fp8kv(q, torch.from_numpy(kv8).to(DEV), torch.from_numpy(sc).to(DEV),
+                                      torch.from_numpy(x["idx"]).to(DEV),
+                                      torch.from_numpy(x["sink"]).to(DEV), x["scale"])
+    torch.cuda.synchronize()
+    O, L = fp8kv.sparse_mla_fwd_fp8kv(x["q"], kv8, sc, x["idx"], x["sink"], x["scale"])
+    # bf16 output rounding grows with |O|: the O bar scales with the largest magnitude
+    res = compare(out, lse, O, L, o_tol=2e-2 * max(1.0, float(np.abs(O).max())))
+    print(variant, res, "max|O|", float(np.abs(O).max()))
+
+
 @pytest.mark.parametrize("T", [1, 4, 16])
 def test_fp8_decode_sized(B, T):
     cfg = synth.CONFIGS[f"decode_h16_t{T}"]
