@@ -405,8 +405,9 @@ def measure_backward(name: str, args, dev, flush, stream, peaks: dict) -> dict:
     t_flop = flops / (peaks["bf16_tflops"] * 1e12)
     t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
     e = {"workload": workload_desc(cfg) + " (backward: dq, dkv, dsink)",
-         "kernels": "bwd_delta, bwd_dq (mma.sync), bwd_interm (mma.sync), inverted index "
-                    "(count, scan, fill), bwd_gather, bwd_dsink",
+         "kernels": "bwd_delta, bwd_compact, bwd_sdp_tc / bwd_dq_tc / bwd_interm_tc (tcgen05; "
+                    "bwd_dq / bwd_interm on mma.sync when H < 128), inverted index (count, scan, "
+                    "fill), bwd_gather, bwd_dsink",
          "ms_per_call": med, "ms_min": min(ms), "ms_max": max(ms), "steps": len(ms),
          "tflops": flops / (med * 1e-3) / 1e12,
          "tflops_all_slots": flops_all / (med * 1e-3) / 1e12,
