@@ -78,7 +78,8 @@ __device__ __forceinline__ bool wait_tc(uint32_t bar, uint32_t parity, TcBars* b
 __global__ void __launch_bounds__(kThreadsTc, 2)
     bwd_interm_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
                          const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_q, const BwdParams p, int ntile) {
+                         const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_out, const BwdParams p, int ntile) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   TcBars* b = reinterpret_cast<TcBars*>(base + kBarOffTc);
@@ -155,9 +156,43 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     if (!ok) wait_tc(bar_addr_tc(b->drain), 0, b, true);   // MMAs issued so far completed
   }
   __syncwarp();
-  // epilogue: thread = TMEM lane = slot of the tile; bf16 rows to the workspace
+  // epilogue: thread = TMEM lane = slot of the tile; bf16 rows to the workspace.
+  // When the tile's 128 rows lie inside the token's topk rows (rows past the
+  // valid count are never read), the tile is staged in the finished ring
+  // (four 64-column blocks, 128-byte swizzle) and stored by four 2-D TMA
+  // boxes: a warp's row-per-lane stores would touch 32 lines per instruction.
   const bool done = __all_sync(0xffffffffu, wait_tc(bar_addr_tc(b->done), 0, b, false));
-  if (done) {
+  const bool boxed = (tile + 1) * kM <= p.topk;
+  if (done && boxed) {
+    tc_fence_after();
+    const int r = 32 * warp + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+#pragma unroll 1
+    for (int cc = 0; cc < kNh / 32; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(tl + 32 * cc, v);
+      tmem_wait_ld();
+      // columns 32 cc .. +31: block cc / 2, 16-byte chunks 4 (cc & 1) .. +3 of row r
+      const uint32_t rowa = sbase + (cc >> 1) * (kM * 128) + r * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(rowa + ((((cc & 1) * 4 + q) ^ (r & 7)) << 4),
+                     make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
+    }
+    fence_proxy_async_smem();   // the staged tile is read by the TMA (async proxy)
+  }
+  if (boxed) {
+    __syncthreads();
+    if (done && threadIdx.x == 0) {
+#pragma unroll
+      for (int j = 0; j < kNh / 64; ++j) tma_store_2d(&tm_out, sbase + j * (kM * 128), kNh * dh + 64 * j, row0);
+      bulk_commit();
+      bulk_wait<0>();   // the boxes are written before the CTA exits
+    }
+  } else if (done) {
     tc_fence_after();
     const int r = 32 * warp + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
@@ -205,7 +240,7 @@ constexpr uint32_t kDqBarOff = 2 * kDqStage;
 constexpr uint32_t kDqSmem = kDqBarOff + 128 + 1024;
 
 __global__ void __launch_bounds__(kDqThreads, 2)
-    bwd_dq_tc_kernel(const BwdParams p) {
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   TcBars* b = reinterpret_cast<TcBars*>(base + kDqBarOff);
@@ -299,21 +334,40 @@ __global__ void __launch_bounds__(kDqThreads, 2)
   if (warp < 4) {
     // epilogue: thread = TMEM lane = head; its 256 dq columns in fp32
     const bool done = __all_sync(0xffffffffu, wait_tc(bar_addr_tc(b->done), 0, b, false));
-    if (done) {
-      tc_fence_after();
-      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-      float4* o = reinterpret_cast<float4*>(dq + int64_t(tid) * kHeadDim);
+    // the 128 x 256 fp32 tile goes out through the finished ring in two 128-column
+    // passes, each four 32-column boxes (128-byte swizzle) stored by 2-D TMA: a
+    // warp's row-per-lane stores would touch 32 lines per instruction
+    tc_fence_after();
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const int r = tid;
 #pragma unroll 1
-      for (int cc = 0; cc < kNh / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(tl + 32 * cc, v);
-        tmem_wait_ld();
+    for (int pass = 0; pass < 2; ++pass) {
+      if (done) {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tl + 128 * pass + 32 * cc, v);
+          tmem_wait_ld();
+          const uint32_t rowa = sbase + cc * (kH * 128) + r * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          o[8 * cc + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                      __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(rowa + ((q ^ (r & 7)) << 4),
+                         make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        }
+        fence_proxy_async_smem();   // the staged boxes are read by the TMA (async proxy)
       }
+      named_bar_sync(1, 128);
+      if (done && tid == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tma_store_2d(&tm_dq, sbase + j * (kH * 128), kNh * dh + 128 * pass + 32 * j,
+                       static_cast<int>(t * kH));
+        bulk_commit();
+        bulk_wait_read<0>();   // the boxes have left shared memory
+      }
+      named_bar_sync(1, 128);
     }
+    if (done && tid == 0) bulk_wait<0>();   // written before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -365,7 +419,8 @@ __device__ __forceinline__ bool wait_sd(uint32_t bar, uint32_t parity, SdBars* b
 
 __global__ void __launch_bounds__(kSdThreads, 2)
     bwd_sdp_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_do, const BwdParams p, int ntile) {
+                      const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_pds, const BwdParams p, int ntile) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   SdBars* b = reinterpret_cast<SdBars*>(base + kSdBarOff);
@@ -472,8 +527,58 @@ __global__ void __launch_bounds__(kSdThreads, 2)
       wait_sd(bar_addr_tc(b->tma[c & 1]), (c >> 1) & 1, b, true);
   }
   __syncwarp();
+  // When the tile's 128 rows lie inside the token's topk rows (rows past the
+  // valid count are never read), the [P | dS'] tile is staged in the finished
+  // ring (four 64-column blocks, 128-byte swizzle) and stored by four 2-D TMA
+  // boxes: a warp's row-per-lane stores would touch 32 lines per instruction.
+  const bool boxed = (tile + 1) * kSdM <= p.topk;
+  bool done = true;
   if (warp < 4) {
-    const bool done = __all_sync(0xffffffffu, wait_sd(bar_addr_tc(b->done), 0, b, false));
+    done = __all_sync(0xffffffffu, wait_sd(bar_addr_tc(b->done), 0, b, false));
+    if (done && boxed) {
+      tc_fence_after();
+      const int r = tid;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+      const float sl2 = p.scale * kLog2e;
+#pragma unroll 1
+      for (int hc = 0; hc < kH / 32; ++hc) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tl + 32 * hc, sv);
+        tmem_ld32(tl + kH + 32 * hc, dv);
+        tmem_wait_ld();
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = 32 * hc + 2 * i;
+          const float p0 = ex2(__uint_as_float(sv[2 * i]) * sl2 - lse2[h]);
+          const float p1 = ex2(__uint_as_float(sv[2 * i + 1]) * sl2 - lse2[h + 1]);
+          pw[i] = pack_bf16x2(p0, p1);
+          dw[i] = pack_bf16x2(p.scale * p0 * (__uint_as_float(dv[2 * i]) - dlt[h]),
+                              p.scale * p1 * (__uint_as_float(dv[2 * i + 1]) - dlt[h + 1]));
+        }
+        // P columns 32 hc .. +31: block hc / 2; dS' the same two blocks further
+        const uint32_t rp = sbase + (hc >> 1) * (kSdM * 128) + r * 128;
+        const uint32_t rd = rp + 2 * (kSdM * 128);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t ch = ((((hc & 1) * 4 + q) ^ (r & 7)) << 4);
+          st_shared_v4(rp + ch, make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]));
+          st_shared_v4(rd + ch, make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]));
+        }
+      }
+      fence_proxy_async_smem();   // the staged tile is read by the TMA (async proxy)
+    }
+  }
+  if (boxed) {
+    __syncthreads();
+    if (done && tid == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tma_store_2d(&tm_pds, sbase + j * (kSdM * 128), 64 * j, static_cast<int>(t * p.topk + slot0));
+      bulk_commit();
+      bulk_wait<0>();   // the boxes are written before the CTA exits
+    }
+  } else if (warp < 4) {
     if (done) {
       tc_fence_after();
       const int r = tid;
@@ -530,16 +635,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tc() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a [rows, cols] row-major matrix, 128-byte swizzle.
+// 2-D tensor map over a [rows, cols] row-major bf16 (or fp32) matrix, 128-byte swizzle.
 bool make_map_2d(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
-                 uint32_t box_cols, uint32_t box_rows) {
+                 uint32_t box_cols, uint32_t box_rows, bool fp32 = false) {
   auto fn = encode_tc();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * (fp32 ? 4 : 2))};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+  return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -552,15 +658,16 @@ int launch_bwd_interm_tc(const BwdParams& p, void* stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemTc));
   if (e != cudaSuccess) return static_cast<int>(e);
-  CUtensorMap ta, tdo, tq;
+  CUtensorMap ta, tdo, tq, to;
   if (!make_map_2d(&ta, p.pds, uint64_t(p.T) * p.topk, 2 * kH, 64, kM) ||
       !make_map_2d(&tdo, p.dout, uint64_t(p.T) * kH, kHeadDim, 64, 64) ||
-      !make_map_2d(&tq, p.q, uint64_t(p.T) * kH, kHeadDim, 64, 64))
+      !make_map_2d(&tq, p.q, uint64_t(p.T) * kH, kHeadDim, 64, 64) ||
+      !make_map_2d(&to, p.interm, uint64_t(p.T) * p.topk, kHeadDim, 64, kM))
     return static_cast<int>(cudaErrorInvalidValue);
   const int ntile = (p.topk + kM - 1) / kM;
   const int64_t blocks = p.T * ntile * 2;
   kern<<<static_cast<unsigned>(blocks), kThreadsTc, kSmemTc, static_cast<cudaStream_t>(stream)>>>(
-      ta, tdo, tq, p, ntile);
+      ta, tdo, tq, to, p, ntile);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -570,7 +677,10 @@ int launch_bwd_dq_tc(const BwdParams& p, void* stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kDqSmem));
   if (e != cudaSuccess) return static_cast<int>(e);
-  kern<<<static_cast<unsigned>(p.T * 2), kDqThreads, kDqSmem, static_cast<cudaStream_t>(stream)>>>(p);
+  CUtensorMap tdq;
+  if (!make_map_2d(&tdq, p.dq, uint64_t(p.T) * kH, kHeadDim, 32, kH, /*fp32=*/true))
+    return static_cast<int>(cudaErrorInvalidValue);
+  kern<<<static_cast<unsigned>(p.T * 2), kDqThreads, kDqSmem, static_cast<cudaStream_t>(stream)>>>(tdq, p);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -580,13 +690,14 @@ int launch_bwd_sdp_tc(const BwdParams& p, void* stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSdSmem));
   if (e != cudaSuccess) return static_cast<int>(e);
-  CUtensorMap tq, tdo;
+  CUtensorMap tq, tdo, tp;
   if (!make_map_2d(&tq, p.q, uint64_t(p.T) * kH, kHeadDim, 64, kH) ||
-      !make_map_2d(&tdo, p.dout, uint64_t(p.T) * kH, kHeadDim, 64, kH))
+      !make_map_2d(&tdo, p.dout, uint64_t(p.T) * kH, kHeadDim, 64, kH) ||
+      !make_map_2d(&tp, p.pds, uint64_t(p.T) * p.topk, 2 * kH, 64, kSdM))
     return static_cast<int>(cudaErrorInvalidValue);
   const int ntile = (p.topk + kSdM - 1) / kSdM;
   kern<<<static_cast<unsigned>(p.T * ntile), kSdThreads, kSdSmem,
-         static_cast<cudaStream_t>(stream)>>>(tq, tdo, p, ntile);
+         static_cast<cudaStream_t>(stream)>>>(tq, tdo, tp, p, ntile);
   return static_cast<int>(cudaGetLastError());
 }
 
