@@ -487,6 +487,12 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTileN, false, false);
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
   constexpr int kRing = 8;   // issued-S tiles awaiting their P.V (at most kSBufs + 2)
+  // Operand descriptors are built once and advanced by adding (byte offset / 16)
+  // to their start-address field (shared addresses < 256 KB: no carry out of it):
+  // a thread issuing tcgen05.mma back to back is bound by its own issue path.
+  const uint64_t d_k0 = sdesc_sw128(sbase + kKVOff, 16, 1024);     // stage 0, K-major
+  const uint64_t d_v0 = sdesc_sw128(sbase + kKVOff, 8192, 1024);   // stage 0, MN-major
+  const uint64_t d_q0 = sdesc_sw128(sbase + kQOff, 16, 1024);
 
   // S side: token walk
   int64_t tok = cid;
@@ -514,14 +520,13 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
         SMLA_TL(1, pg, 3);
         tc_fence_after();
         const uint32_t s = pg % kStages;
-        const uint32_t kv = sbase + kKVOff + s * kStageBytes;
         const uint32_t ptm = tmem + kTmemP + (pg % kPBufs) * 32;   // P: 64 bf16 = 32 columns
+        // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart; a K
+        // step is 16 slot rows (2 KB = 128 in the descriptor's start-address field)
+        const uint64_t vd = d_v0 + s * (kStageBytes >> 4);
+        mma_bf16_ts(tmem, ptm, vd, kIdescO, jj > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart
-          const uint64_t bd = sdesc_sw128(kv + kk * 16 * 128, 8192, 1024);
-          mma_bf16_ts(tmem, ptm + kk * 8, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kTileN / 16; ++kk) mma_bf16_ts(tmem, ptm + kk * 8, vd + kk * 128, kIdescO, 1u);
         mma_commit(bar_addr(b->kv_empty[s]));
         mma_commit(bar_addr(b->pv_done[pg % kPBufs]));
         SMLA_TL(1, pg, 4);
@@ -588,16 +593,17 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
              mbar_test_wait(bar_addr(b->s_free[(sg - 1) & 1]), ((sg - 1) >> 1) & 1))) {
           SMLA_TL(1, sg, 1);
           tc_fence_after();
-          const uint32_t kv = sbase + kKVOff + s * kStageBytes;
+          // K rows as K-major B (64-column blocks 8 KB apart); a K step of 16 elements is
+          // 32 B inside a 128 B row (2 in the descriptor's start-address field)
+          const uint64_t kd = d_k0 + s * (kStageBytes >> 4);
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk) {
-            const uint32_t koff = (kk & 3) * 32;   // 16 K elements = 32 B inside a 128 B row
-            const uint64_t bd = sdesc_sw128(kv + (kk >> 2) * 8192 + koff, 16, 1024);
+            const uint64_t bd = kd + (kk >> 2) * 512 + (kk & 3) * 2;
             if (kk < 8) {   // Q columns 0-127 from TMEM
               mma_bf16_ts(tmem + kTmemS + sb * kTileN, tmem + kTmemQ + 8 * kk, bd, kIdescS,
                           kk > 0 ? 1u : 0u);
-            } else {        // Q columns 128-255 from shared memory
-              const uint64_t a = sdesc_sw128(sbase + kQOff + ((kk - 8) >> 2) * 16384 + koff, 16, 1024);
+            } else {        // Q columns 128-255 from shared memory (16 KB per 64 columns)
+              const uint64_t a = d_q0 + ((kk - 8) >> 2) * 1024 + (kk & 3) * 2;
               mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, bd, kIdescS, 1u);
             }
           }
