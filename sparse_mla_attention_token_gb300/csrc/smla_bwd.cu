@@ -538,8 +538,12 @@ __global__ void bwd_csr_fill_kernel(const BwdParams p) {
 
 // ------------------------------------------------------------------ 5. dkv gather
 // One CTA of 128 threads per kv row: 4 columns each (one 8-byte load of bf16
-// per entry), fp32 sums of the row's interm entries in list order.
+// per entry), fp32 sums of the row's interm entries in list order.  Entries go
+// 16 at a time, and the next 16 list entries are loaded while the current rows
+// are summed, so a long row (a pool row named by many tokens) keeps 16 rows and
+// the next index chunk in flight instead of paying two latencies per chunk.
 __global__ void __launch_bounds__(128) bwd_gather_kernel(const BwdParams p) {
+  constexpr int kU = 16;
   const int64_t r = blockIdx.x;
   const int b = p.row_cnt[r], e_end = p.row_cnt[r + 1];
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -548,12 +552,21 @@ __global__ void __launch_bounds__(128) bwd_gather_kernel(const BwdParams p) {
     acc.x += bf16_lo(v.x); acc.y += bf16_hi(v.x); acc.z += bf16_lo(v.y); acc.w += bf16_hi(v.y);
   };
   int i = b;
-  for (; i + 8 <= e_end; i += 8) {
-    uint2 v[8];
+  int nx[kU];
+  if (i + kU <= e_end) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = src[int64_t(p.list[i + u]) * (kHeadDim / 4)];
+    for (int u = 0; u < kU; ++u) nx[u] = p.list[i + u];
+  }
+  for (; i + kU <= e_end; i += kU) {
+    uint2 v[kU];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) add(v[u]);
+    for (int u = 0; u < kU; ++u) v[u] = src[int64_t(nx[u]) * (kHeadDim / 4)];
+    if (i + 2 * kU <= e_end) {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) nx[u] = p.list[i + kU + u];
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) add(v[u]);
   }
   for (; i < e_end; ++i) add(src[int64_t(p.list[i]) * (kHeadDim / 4)]);
   reinterpret_cast<float4*>(p.dkv + r * kHeadDim)[threadIdx.x] = acc;
