@@ -462,21 +462,28 @@ __global__ void __launch_bounds__(kSdThreads, 2)
   const int* crow = p.crow + t * p.topk;
 
   if (warp < 4) {
-    // gather: thread = slot row r of the tile; 8 chunks of 16 B per 64-column chunk
-    const int r = tid;
-    const bool v = slot0 + r < nv;
-    const char* src_row =
-        static_cast<const char*>(p.kv) + (v ? int64_t(crow[slot0 + r]) * 1024 : 0);
+    // gather: a 64-column chunk is 128 rows x 8 pieces of 16 B; copy j of this thread
+    // is piece q = tid % 8 of row 16 j + tid / 8, so 8 lanes read one row's 128
+    // contiguous bytes and a warp instruction four whole lines
+    const int q = tid & 7, r0 = tid >> 3;
+    const char* src_row[8];
+    bool vr[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = 16 * j + r0;
+      vr[j] = slot0 + r < nv;
+      src_row[j] = static_cast<const char*>(p.kv) + (vr[j] ? int64_t(crow[slot0 + r]) * 1024 : 0) + q * 16;
+    }
+    const uint32_t dst_off = r0 * 128 + ((q ^ (r0 & 7)) << 4);   // row 16 j + r0 adds 2 KB j
     bool ok = true;
     for (int c = 0; c < kSdChunks && ok; ++c) {
       const int s = c & 1;
       if (c >= 2 &&
           !(ok = __all_sync(0xffffffffu, wait_sd(bar_addr_tc(b->empty[s]), ((c >> 1) - 1) & 1, b, false))))
         break;
-      const uint32_t dst = sbase + s * kSdStage + r * 128;
+      const uint32_t dst = sbase + s * kSdStage + dst_off;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        cp_async_16(dst + ((q ^ (r & 7)) << 4), src_row + c * 128 + q * 16, v ? 16u : 0u);
+      for (int j = 0; j < 8; ++j) cp_async_16(dst + j * 2048, src_row[j] + c * 128, vr[j] ? 16u : 0u);
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async_smem();
