@@ -59,7 +59,8 @@ struct TcBars {
   int abort_flag;
 };
 
-__device__ __forceinline__ bool wait_tc(uint32_t bar, uint32_t parity, TcBars* b, bool drain) {
+template <typename BarsT>
+__device__ __forceinline__ bool wait_tc(uint32_t bar, uint32_t parity, BarsT* b, bool drain) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t n = 1;; ++n) {
@@ -224,26 +225,36 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
 }
 
 // dq = scale * dS . K for H = 128: M = 128 heads, N = 256 (a D half), K = the
-// token's valid slots in 64-slot chunks.  A = (scale dS)^T, MN-major: each
+// token's valid slots in 32-slot chunks.  A = (scale dS)^T, MN-major: each
 // slot's 128 dS' values (256 bytes of the workspace row) as two 128-byte rows of
 // two 64-head blocks; B = the gathered kv half rows, MN-major (the forward's
-// stage layout).  Warps 0-3 gather both with 16-byte cp.async into a two-stage
-// ring (slots past the valid count zero-filled, so the uninitialised workspace
-// past them never enters a sum) and then run the epilogue; warp 4 lane 0 owns
-// TMEM and issues four M128 N256 K16 MMAs per chunk.
+// stage layout).  Warps 0-3 gather both with 16-byte cp.async into a four-stage
+// ring, up to three chunks in flight per thread (slots past the valid count
+// zero-filled, so the uninitialised workspace past them never enters a sum),
+// and then run the epilogue; warp 4 lane 0 owns TMEM and issues two M128 N256
+// K16 MMAs per chunk.
 constexpr int kDqThreads = 160;
-constexpr int kDqChunk = 64;                         // slots per chunk
-constexpr uint32_t kDqA = kDqChunk * kH * 2;         // 16 KB: [2 head blocks][64 slots][128 B]
-constexpr uint32_t kDqB = kDqChunk * kNh * 2;        // 32 KB: [4 column blocks][64 slots][128 B]
+constexpr int kDqChunk = 32;                         // slots per chunk
+constexpr int kDqStages = 4;
+constexpr uint32_t kDqBlk = kDqChunk * 128;          // 4 KB: one 64-element block of 32 slots
+constexpr uint32_t kDqA = kDqChunk * kH * 2;         // 8 KB: [2 head blocks][32 slots][128 B]
+constexpr uint32_t kDqB = kDqChunk * kNh * 2;        // 16 KB: [4 column blocks][32 slots][128 B]
 constexpr uint32_t kDqStage = kDqA + kDqB;
-constexpr uint32_t kDqBarOff = 2 * kDqStage;
+constexpr uint32_t kDqBarOff = kDqStages * kDqStage;   // 96 KB (also the epilogue's staging)
 constexpr uint32_t kDqSmem = kDqBarOff + 128 + 1024;
+
+struct DqBars {
+  uint64_t full[kDqStages], empty[kDqStages], done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(DqBars) <= 128, "barriers fit their slot");
 
 __global__ void __launch_bounds__(kDqThreads, 2)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  TcBars* b = reinterpret_cast<TcBars*>(base + kDqBarOff);
+  DqBars* b = reinterpret_cast<DqBars*>(base + kDqBarOff);
   const uint32_t sbase = smem_u32(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int dh = blockIdx.x & 1;
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(kDqThreads, 2)
     return;
   }
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kDqStages; ++s) {
       mbar_init(bar_addr_tc(b->full[s]), 128);     // the four gather warps
       mbar_init(bar_addr_tc(b->empty[s]), 1);
     }
@@ -281,50 +292,86 @@ __global__ void __launch_bounds__(kDqThreads, 2)
     const char* pds = static_cast<const char*>(p.pds) + t * p.topk * int64_t(2 * kH * 2);
     const int* crow = p.crow + t * p.topk;
     const char* kvb = static_cast<const char*>(p.kv) + kNh * 2 * dh;   // this CTA's D half
+    // copies of a chunk: A k = 0..3 is piece qa = tid % 16 of slot 8 k + tid / 16 (16
+    // lanes read one slot's 256 dS' bytes); B k = 0..7 is piece qb = tid % 32 of slot
+    // 4 k + tid / 32 (a warp reads one kv half row)
+    const int qa = tid & 15, ra = tid >> 4, qb = lane, rb = warp;
+    const uint32_t a_off = (qa >> 3) * kDqBlk + ra * 128 + (((qa & 7) ^ (ra & 7)) << 4);
+    const uint32_t b_off = kDqA + (qb >> 3) * kDqBlk + rb * 128;   // + row 4 k, swizzled below
+    // A chunk's copies are counted on its barrier once kDepth - 1 later chunks are
+    // issued; before any wait that may block, the pending chunks are counted first
+    // (the slot waited for is freed by MMAs that need them).  Pending chunks are
+    // consecutive, from `first`.
+    constexpr int kDepth = 3;
+    int first = 0, npend = 0;
+    auto count_oldest = [&]() {
+      mbar_arrive(bar_addr_tc(b->full[first % kDqStages]));
+      ++first;
+      --npend;
+    };
+    auto flush = [&]() {
+      if (npend > 0) {
+        cp_async_wait<0>();
+        fence_proxy_async_smem();   // visible to the tensor core's async proxy
+        while (npend > 0) count_oldest();
+      }
+    };
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int s = c & 1;
-      if (c >= 2 &&
-          !(ok = __all_sync(0xffffffffu, wait_tc(bar_addr_tc(b->empty[s]), ((c >> 1) - 1) & 1, b, false))))
-        break;
-      const uint32_t st = sbase + s * kDqStage;
-      // A: slot r's dS' (heads 0-127) = 16 chunks: head block hb = chunk / 8
-      for (int i = tid; i < kDqChunk * 16; i += 128) {
-        const int r = i >> 4, q = i & 15;
-        const int slot = c * kDqChunk + r;
-        const bool v = slot < nv;
-        const char* src = v ? pds + int64_t(slot) * (2 * kH * 2) + kH * 2 + q * 16 : pds;
-        cp_async_16(st + (q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4), src, v ? 16u : 0u);
+      const int s = c % kDqStages;
+      if (c >= kDqStages) {
+        const uint32_t eb = bar_addr_tc(b->empty[s]), ep = ((c / kDqStages) - 1) & 1;
+        if (!mbar_test_wait(eb, ep)) {
+          flush();
+          if (!(ok = wait_tc(eb, ep, b, false))) break;
+        }
       }
-      // B: slot r's kv half row = 32 chunks: column block cb = chunk / 8
-      for (int i = tid; i < kDqChunk * 32; i += 128) {
-        const int r = i >> 5, q = i & 31;
-        const int slot = c * kDqChunk + r;
+      const uint32_t st = sbase + s * kDqStage;
+      const int s0 = c * kDqChunk;
+      int rowb[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int slot = s0 + 4 * k + rb;
+        rowb[k] = slot < nv ? crow[slot] : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int slot = s0 + 8 * k + ra;
         const bool v = slot < nv;
-        const char* src = v ? kvb + int64_t(crow[slot]) * 1024 + q * 16 : kvb;
-        cp_async_16(st + kDqA + (q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4), src,
-                    v ? 16u : 0u);
+        const char* src = v ? pds + int64_t(slot) * (2 * kH * 2) + kH * 2 + qa * 16 : pds;
+        cp_async_16(st + a_off + k * 8 * 128, src, v ? 16u : 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const bool v = rowb[k] >= 0;
+        const char* src = v ? kvb + int64_t(rowb[k]) * 1024 + qb * 16 : kvb;
+        // row 4 k + rb: its low three bits are rb + 4 (k & 1)
+        cp_async_16(st + b_off + k * 4 * 128 + (((qb & 7) ^ ((rb + 4 * k) & 7)) << 4), src, v ? 16u : 0u);
       }
       cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();   // visible to the tensor core's async proxy
-      mbar_arrive(bar_addr_tc(b->full[s]));
+      if (npend == 0) first = c;
+      if (++npend == kDepth) {
+        cp_async_wait<kDepth - 1>();   // the oldest pending chunk has landed
+        fence_proxy_async_smem();
+        count_oldest();
+      }
     }
+    flush();
     cp_async_wait<0>();
   } else if (lane == 0) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(kH, kNh, true, true);
+    // MN-major A and B: 64-element blocks kDqBlk apart, 8-slot groups 1 KB apart; a K
+    // step is 16 slots (2 KB, 128 in the descriptor's start-address field)
+    const uint64_t d0 = sdesc_sw128(sbase, kDqBlk, 1024);
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int s = c & 1;
-      if (!(ok = wait_tc(bar_addr_tc(b->full[s]), (c >> 1) & 1, b, false))) break;
+      const int s = c % kDqStages;
+      if (!(ok = wait_tc(bar_addr_tc(b->full[s]), (c / kDqStages) & 1, b, false))) break;
       tc_fence_after();
-      const uint32_t st = sbase + s * kDqStage;
+      const uint64_t ad = d0 + s * (kDqStage >> 4), bd = ad + (kDqA >> 4);
 #pragma unroll
-      for (int kk = 0; kk < kDqChunk / 16; ++kk) {
-        const uint64_t ad = sdesc_sw128(st + kk * 16 * 128, 8192, 1024);          // MN-major A
-        const uint64_t bd = sdesc_sw128(st + kDqA + kk * 16 * 128, 8192, 1024);   // MN-major B
-        mma_bf16_ss(tmem, ad, bd, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < kDqChunk / 16; ++kk)
+        mma_bf16_ss(tmem, ad + kk * 128, bd + kk * 128, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
       mma_commit(bar_addr_tc(b->empty[s]));
     }
     mma_commit(bar_addr_tc(ok ? b->done : b->drain));
