@@ -522,20 +522,39 @@ __global__ void __launch_bounds__(kSdThreads, 2)
       src_row[j] = static_cast<const char*>(p.kv) + (vr[j] ? int64_t(crow[slot0 + r]) * 1024 : 0) + q * 16;
     }
     const uint32_t dst_off = r0 * 128 + ((q ^ (r0 & 7)) << 4);   // row 16 j + r0 adds 2 KB j
+    // a chunk's copies are counted once the next chunk is issued (two in flight per
+    // thread); before a wait that may block, the pending chunk is counted first
+    int pend = -1;
+    auto flush = [&]() {
+      if (pend >= 0) {
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(bar_addr_tc(b->full[pend & 1]));
+        pend = -1;
+      }
+    };
     bool ok = true;
     for (int c = 0; c < kSdChunks && ok; ++c) {
       const int s = c & 1;
-      if (c >= 2 &&
-          !(ok = __all_sync(0xffffffffu, wait_sd(bar_addr_tc(b->empty[s]), ((c >> 1) - 1) & 1, b, false))))
-        break;
+      if (c >= 2) {
+        const uint32_t eb = bar_addr_tc(b->empty[s]), ep = ((c >> 1) - 1) & 1;
+        if (!mbar_test_wait(eb, ep)) {
+          flush();
+          if (!(ok = wait_sd(eb, ep, b, false))) break;
+        }
+      }
       const uint32_t dst = sbase + s * kSdStage + dst_off;
 #pragma unroll
       for (int j = 0; j < 8; ++j) cp_async_16(dst + j * 2048, src_row[j] + c * 128, vr[j] ? 16u : 0u);
       cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(bar_addr_tc(b->full[s]));
+      if (pend >= 0) {
+        cp_async_wait<1>();   // the previous chunk has landed
+        fence_proxy_async_smem();
+        mbar_arrive(bar_addr_tc(b->full[pend & 1]));
+      }
+      pend = c;
     }
+    flush();
     cp_async_wait<0>();
   } else if (lane == 0) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(kSdM, kH, false, false);
