@@ -112,6 +112,10 @@ CONFIGS = {
     # the h128 recipe at a quarter of the tokens: the small case for Nsight Compute captures
     "h128_small": Config("h128_small", T=1024, H=128, pool=256, ratio=4, topk=512, window=128,
                          seed=3),
+    # the small_head recipe at a quarter of the tokens (inputs and output ~150 MB > L2), for
+    # the same purpose
+    "small_head_4k": Config("small_head_4k", T=4096, H=16, pool=1024, ratio=4, topk=640,
+                            window=128, seed=1),
     # The GLM-shaped call of "Tuned sparse MLA prefill for DSv4.1-Flash TP4" (review
     # thread: 16 heads per rank, D=512, top-k 2048, a 16K-row call, a KV pool over
     # 2 GiB): the sequence's rows start 2^21 rows (2 GiB) into the pool, so every
