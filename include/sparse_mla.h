@@ -174,9 +174,9 @@ smla_status_t sparse_mla_fwd_fp8kv(const void* q, const void* kv_fp8, const floa
  * sparse_mla_fwd_static_scratch -- the split-TOPK path without any allocation.
  *
  * The pages have no counterpart to this entry point.  It exists for callers
- * that must not allocate device memory while they run: code recorded into a
- * stream capture that must not contain allocation steps, serving loops with a
- * fixed memory budget, and hosts whose allocator is owned by another runtime.
+ * that must not allocate device memory while they run: serving loops with a
+ * fixed memory budget, code running inside a window in which no allocation may
+ * happen, and hosts whose allocator is owned by another runtime.
  * sparse_mla_fwd_ex allocates the split path's partial results on every call;
  * this entry point keeps them in one fixed array inside the library instead
  * (8192 x 2052 bytes = 16,809,984 bytes of device memory, held by every GPU
@@ -193,8 +193,8 @@ smla_status_t sparse_mla_fwd_fp8kv(const void* q, const void* kv_fp8, const floa
  *                been reset) looks up the array's device address.  With CUDA's
  *                lazy module loading that lookup is what loads the library's
  *                device code and maps the array, an allocation made by the
- *                driver: make the first call before any stream capture and
- *                outside any no-allocation window.
+ *                driver: make the first call outside any window in which no
+ *                allocation may happen.
  *   Sharing      every call uses the same array: calls whose kernels overlap
  *                on the GPU (other streams, other host threads) race and give
  *                wrong results.  Serialise them on one stream.  No state

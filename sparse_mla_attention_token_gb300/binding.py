@@ -223,8 +223,8 @@ def sparse_mla_fwd_static_scratch(q, kv, topk_indices, out, lse, attn_sink=None,
                                   stream=None):
     """The split-TOPK forward with no device allocation at all; returns ``(out, lse)``.
 
-    For callers that may not allocate while they run (a stream being
-    captured, a fixed memory budget, an allocator owned by someone else):
+    For callers that may not allocate while they run (a fixed memory budget, a
+    window in which no allocation may happen, an allocator owned by someone else):
     ``out`` and ``lse`` must be passed in, and the split partials live in the
     library's own 16 MiB static array.  ``num_splits * T * H`` may not exceed
     8192.  Calls that overlap on the GPU share that array and race; run them

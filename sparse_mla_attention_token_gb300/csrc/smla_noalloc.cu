@@ -13,8 +13,8 @@
 //     process exits;
 //   * the first call on a device looks up the array's device address (one
 //     cudaGetSymbolAddress; under lazy module loading that lookup loads the
-//     device code and maps the array), so make that first call before any
-//     stream capture;
+//     device code and maps the array), so make that first call outside any
+//     window in which no allocation may happen;
 //   * the address is cached per device together with the id of the context it
 //     was taken in; after a device reset the context id changes and the next
 //     call looks the address up again instead of using a stale one;

@@ -1,8 +1,8 @@
 """The allocation-free entry point against the regular one (needs a GB300).
 
 ``sparse_mla_fwd_static_scratch`` serves callers that may not allocate device
-memory while they run (work recorded into a stream capture, a fixed memory
-budget, an allocator owned by another runtime): it runs the split-TOPK path
+memory while they run (a fixed memory budget, a window in which no allocation
+may happen, an allocator owned by another runtime): it runs the split-TOPK path
 with its partial results in the library's fixed scratch array.  Two calls in a
 row, with different shapes and inputs, must each agree with
 ``sparse_mla_fwd_ex`` (the same split count: the same kernels, so bit for
