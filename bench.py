@@ -23,8 +23,9 @@ workload and decode-sized calls of 1-16 tokens), each timed the same way (L2
 flushed before every timed call, CUDA events on the launching stream), with
 its roofline fractions and the fp64 oracle timed on a bounded token sample;
 ``fp8_small_head`` / ``fp8_sweep_k640``: the same workloads on an fp8 KV
-cache; and ``bwd_h128``: the training backward on the T=4096 H=128 topk=512
-workload.
+cache; and ``bwd_h128`` / ``bwd_h128_k1024`` / ``bwd_h128_t8192``: the training
+backward on the page's three measured shapes (T=4096 topk=512, T=4096 topk=1024,
+T=8192 topk=512; H=128).
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this op
 has) on bounded token samples of the same workload, on rank 0 only.
@@ -580,7 +581,8 @@ def run_ours(args, cfg) -> None:
         pw_sampler.start()
         p0 = time.time()
         if args.per_workload == "all":
-            names = names + ["fp8_small_head", "fp8_sweep_k640", "bwd_h128"]
+            names = names + ["fp8_small_head", "fp8_sweep_k640", "bwd_h128", "bwd_h128_k1024",
+                             "bwd_h128_t8192"]
         for n in names:
             if n == cfg.name:
                 continue

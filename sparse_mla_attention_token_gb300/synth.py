@@ -109,6 +109,12 @@ CONFIGS = {
     "h128": Config("h128", T=4096, H=128, pool=1024, ratio=4, topk=512, window=128, seed=3),
     "h128_long": Config("h128_long", T=8192, H=128, pool=1024, ratio=8, topk=1024, window=256,
                         index_dtype="int64", kv_offset_bytes=(2 << 30) + 4096, seed=4),
+    # the backward's two other measured shapes ("Sparse MLA training backward",
+    # "Performance"): T=4096 topk=1024 over 5120 kv rows, T=8192 topk=512 over 9216
+    "h128_k1024": Config("h128_k1024", T=4096, H=128, pool=1024, ratio=4, topk=1024, window=128,
+                         seed=6),
+    "h128_t8192": Config("h128_t8192", T=8192, H=128, pool=1024, ratio=8, topk=512, window=128,
+                         seed=7),
     # the h128 recipe at a quarter of the tokens: the small case for Nsight Compute captures
     "h128_small": Config("h128_small", T=1024, H=128, pool=256, ratio=4, topk=512, window=128,
                          seed=3),

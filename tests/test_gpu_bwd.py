@@ -126,6 +126,20 @@ def test_bwd_h128_sampled_rows(B):
     _compare(B, x, synth.make_dout(cfg))
 
 
+@pytest.mark.parametrize("topk,window", [(300, 128), (1024, 256)])
+def test_bwd_h128_tile_boundaries(B, topk, window):
+    # H = 128 on the tcgen05 kernels: topk 300 ends in a partial 128-slot tile (its
+    # rows stored lane by lane, the full tiles by TMA boxes); topk 1024 with int64
+    # indices is the page's second backward shape at reduced T
+    # (2048 earlier context rows: every slot of every token is valid)
+    cfg = synth.CONFIGS["h128"].with_(T=192, pos0=2048, pool=1200, ratio=2, topk=topk,
+                                      window=window, seed=235 + topk)
+    x = synth.make_inputs(cfg)
+    if topk == 1024:
+        x["idx"] = x["idx"].astype(np.int64)
+    _compare(B, x, synth.make_dout(cfg))
+
+
 def test_bwd_unused_rows_are_zero_and_shared_pool(B):
     # the sequence's rows sit 3000 rows into a shared pool; the NaN rows of the
     # other sequences are never read and their gradient rows are exactly zero
