@@ -93,7 +93,9 @@ constexpr uint32_t kQOff = 0;                         // [2 col blocks][128 rows
 constexpr uint32_t kQBytes = 128 * 128 * 2;           // 32 KB: Q columns 0-127 (staged for TMEM), then 128-255
 constexpr uint32_t kKVOff = kQOff + kQBytes;          // [stage][4 col blocks][64 rows][128 B]
 constexpr uint32_t kStageBytes = kTileN * 256 * 2;    // 32 KB
-constexpr uint32_t kXOff = kKVOff + kStages * kStageBytes;   // peer partials: [2][128][64 fp16]
+// peer partials: [2 buffers][8 chunks][128 rows][16 B] (chunk c of row r at c * 2 KB + r * 16,
+// so that a warp's 16-byte stores of one chunk for its 32 rows are 512 contiguous bytes)
+constexpr uint32_t kXOff = kKVOff + kStages * kStageBytes;
 constexpr int kXBufs = 2;
 constexpr uint32_t kXBufBytes = 128 * kTileN * 2;     // 16 KB per buffer
 constexpr uint32_t kStgOff = kXOff + kXBufs * kXBufBytes;    // O store staging: [4 warps][2][32][32 bf16]
@@ -707,7 +709,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
   uint32_t xmax_peer[kXBufs];
 #pragma unroll
   for (int i = 0; i < kXBufs; ++i) {
-    recv_local[i] = sbase + kXOff + i * kXBufBytes + row * 128;
+    recv_local[i] = sbase + kXOff + i * kXBufBytes + row * 16;   // chunk c at + c * 2 KB
     recv_peer[i] = map_peer(recv_local[i], peer);
     xmax_peer[i] = map_peer(sbase + kXMaxOff + (i * 128 + row) * 4, peer);
     xfull_peer[i] = map_peer(bar_addr(b->x_full[i]), peer);
@@ -774,7 +776,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
       if (row == 0) SMLA_TL(3, g, 1);
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        st_async_v4(recv_peer[xb] + ((c ^ (row & 7)) << 4),
+        st_async_v4(recv_peer[xb] + c * 2048,
                     make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]),
                     xfull_peer[xb]);
       st_async_b32(xmax_peer[xb], __float_as_uint(o_own), xfull_peer[xb]);
@@ -790,8 +792,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
       float s[64];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(base + (recv_local[xb] - sbase) +
-                                                        ((c ^ (row & 7)) << 4));
+        const uint4 v = *reinterpret_cast<const uint4*>(base + (recv_local[xb] - sbase) + c * 2048);
         const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
