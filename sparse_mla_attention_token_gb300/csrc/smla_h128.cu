@@ -82,11 +82,12 @@ constexpr int kTileN = 64;            // slots per tile
 constexpr int kStages = 4;
 constexpr int kMaxTopk = 1024;        // row-list capacity (two lists)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 1;
-constexpr int kPBufs = 4;
-constexpr uint32_t kTmemS = 256;      // one S buffer (64 columns); O at 0
-constexpr uint32_t kTmemP = 320;      // four P buffers (32 columns of bf16 pairs each)
-constexpr uint32_t kTmemQ = 448;      // Q columns 0-127 of this CTA's half (64 columns of bf16 pairs)
+constexpr int kSBufs = 2;
+constexpr int kPBufs = 2;
+constexpr uint32_t kTmemS = 256;      // S buffers (64 columns each); O at 0
+constexpr uint32_t kTmemP = kTmemS + kSBufs * 64;   // P buffers (32 columns of bf16 pairs each)
+constexpr uint32_t kTmemQ = kTmemP + kPBufs * 32;   // Q columns 0-127 of this CTA's half (64 columns)
+static_assert(kTmemQ + 64 <= kTmemCols, "TMEM columns");
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kQOff = 0;                         // [2 col blocks][128 rows][128 B]
@@ -589,10 +590,10 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
       } else {
         const uint32_t s = sg % kStages, ph = (sg / kStages) & 1;
         const uint32_t sb = sg % kSBufs;
-        // the S buffer's previous tile, S(sg-1), has been read
+        // the S buffer's previous tile, S(sg - kSBufs), has been read
         if (mbar_test_wait(bar_addr(b->kv_full[s]), ph) &&
-            (sg == 0 ||
-             mbar_test_wait(bar_addr(b->s_free[(sg - 1) & 1]), ((sg - 1) >> 1) & 1))) {
+            (sg < kSBufs ||
+             mbar_test_wait(bar_addr(b->s_free[(sg - kSBufs) & 1]), ((sg - kSBufs) >> 1) & 1))) {
           SMLA_TL(1, sg, 1);
           tc_fence_after();
           // K rows as K-major B (64-column blocks 8 KB apart); a K step of 16 elements is
