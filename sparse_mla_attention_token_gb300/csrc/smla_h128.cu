@@ -514,6 +514,44 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   long long last = clock64();
   while (true) {
     bool progress = false;
+    // ---- the next token's Q (gates its first S): ahead of a ready P.V
+    if (have_meta && q_state < 3) {
+      if (q_state == 0) {
+        // Q columns 0-127 landed (loaded once the previous token's last S completed):
+        // into TMEM, 16 K elements (8 columns) per copy
+        if (mbar_test_wait(bar_addr(b->q_lo_full), qn & 1)) {
+          SMLA_TL(1, sg, 6);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tmem_cp_128x256b(tmem + kTmemQ + 8 * kk,
+                             sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024));
+          mma_commit(bar_addr(b->qcp_done));
+          q_state = 1;
+          progress = true;
+        }
+      } else if (q_state == 1) {
+        // the copies have read the buffer: columns 128-255 into it
+        if (mbar_test_wait(bar_addr(b->qcp_done), qn & 1)) {
+          SMLA_TL(1, sg, 7);
+          mbar_arrive_expect_tx(bar_addr(b->q_hi_full), kQBytes);
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 128 + 64 * cb,
+                        static_cast<int>(tok * 128), bar_addr(b->q_hi_full));
+          ++hi_loads;
+          q_state = 2;
+          progress = true;
+        }
+      } else if (q_state == 2) {
+        if (mbar_test_wait(bar_addr(b->q_hi_full), qn & 1)) {
+          SMLA_TL(1, sg, 5);
+          tc_fence_after();
+          q_state = 3;
+          progress = true;
+        }
+      }
+    }
     // ---- next P.V
     if (pg < sg) {
       const int jj = ring_j[pg % kRing];
@@ -555,38 +593,8 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
             ++it;
           }
         }
-      } else if (q_state == 0) {
-        // Q columns 0-127 landed (loaded once the previous token's last S completed):
-        // into TMEM, 16 K elements (8 columns) per copy
-        if (mbar_test_wait(bar_addr(b->q_lo_full), qn & 1)) {
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tmem_cp_128x256b(tmem + kTmemQ + 8 * kk,
-                             sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024));
-          mma_commit(bar_addr(b->qcp_done));
-          q_state = 1;
-          progress = true;
-        }
-      } else if (q_state == 1) {
-        // the copies have read the buffer: columns 128-255 into it
-        if (mbar_test_wait(bar_addr(b->qcp_done), qn & 1)) {
-          mbar_arrive_expect_tx(bar_addr(b->q_hi_full), kQBytes);
-#pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sbase + kQOff + cb * 16384, tm_q, 256 * int(rank) + 128 + 64 * cb,
-                        static_cast<int>(tok * 128), bar_addr(b->q_hi_full));
-          ++hi_loads;
-          q_state = 2;
-          progress = true;
-        }
-      } else if (q_state == 2) {
-        if (mbar_test_wait(bar_addr(b->q_hi_full), qn & 1)) {
-          SMLA_TL(1, sg, 5);
-          tc_fence_after();
-          q_state = 3;
-          progress = true;
-        }
+      } else if (q_state < 3) {
+        // the Q chain advances above
       } else {
         const uint32_t s = sg % kStages, ph = (sg / kStages) & 1;
         const uint32_t sb = sg % kSBufs;
