@@ -257,6 +257,17 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
   // the next token's list is compacted and its first tile gathered while the
   // current token's last tile is computed, so a token's gather latency hides
   // behind the previous token's work.
+  // this thread's epilogue rows g and g + 8: their sinks (base-2 logits), read
+  // once for all of the CTA's tokens (the head group is fixed), not in every
+  // token's epilogue between its two barriers
+  float sk2[2] = {-INFINITY, -INFINITY};
+  if constexpr (!kSplit) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int r = g + half * 8;
+      if (p.sink != nullptr && r < hvalid) sk2[half] = p.sink[h0 + r] * kLog2e;
+    }
+  }
   load_q(t0);
   int cur = 0;                    // row list of the current token
   int nv_cur = compact(t0, cur);
@@ -353,6 +364,10 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
       for (int ri = 0; ri < kRPH; ++ri) {
         const int srow = hw + ri * kHW;
         if (srow >= kHG) break;   // warp-uniform: kHW divides 16, or whole warps have no row
+        // a warp whose two rows are both past the group's heads (H = 8: warps 4-7)
+        // skips them (warp-uniform test): an MMA row of O depends only on the same
+        // row of P and alpha, and those rows' outputs are never stored
+        if (2 * warp + ri * kHW >= hvalid) continue;
         float a[kCols];
   #pragma unroll
         for (int k = 0; k < kCols; ++k) a[k] = 0.f;
@@ -475,10 +490,10 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
         const int r = g + half * 8;
         const float m = sm.row_m[r], l = sm.row_l[r];
         float m2 = m, l2 = l;
-        if (p.sink != nullptr && r < hvalid) {
-          const float sk = p.sink[h0 + r] * kLog2e;
+        if (sk2[half] != -INFINITY) {
+          const float sk = sk2[half];
           m2 = fmaxf(m, sk);
-          if (m2 != -INFINITY) l2 = l * ex2(m - m2) + ex2(sk - m2);
+          l2 = l * ex2(m - m2) + ex2(sk - m2);
         }
         const bool live = (m2 != -INFINITY) && (l2 > 0.f);
         const float f = live ? ex2(m - m2) / l2 : 0.f;
