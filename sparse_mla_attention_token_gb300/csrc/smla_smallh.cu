@@ -350,12 +350,14 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
         }
       }
       float* sw = sm.sred[warp];
+      const bool hi_row = g + 8 < hvalid;   // rows past the group's heads are never reduced
   #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
         *reinterpret_cast<float2*>(&sw[g * kSredStride + nt * 8 + 2 * tig]) =
             make_float2(s[nt][0], s[nt][1]);
-        *reinterpret_cast<float2*>(&sw[(g + 8) * kSredStride + nt * 8 + 2 * tig]) =
-            make_float2(s[nt][2], s[nt][3]);
+        if (hi_row)
+          *reinterpret_cast<float2*>(&sw[(g + 8) * kSredStride + nt * 8 + 2 * tig]) =
+              make_float2(s[nt][2], s[nt][3]);
       }
       __syncthreads();
 
@@ -488,6 +490,7 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
   #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int r = g + half * 8;
+        if (r >= hvalid) continue;   // never stored (the copy below takes hvalid rows)
         const float m = sm.row_m[r], l = sm.row_l[r];
         float m2 = m, l2 = l;
         if (sk2[half] != -INFINITY) {
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
             *reinterpret_cast<uint32_t*>(&ost[r * kOStride + warp * 64 + nt * 8 + 2 * tig]) =
                 pack_bf16x2(acc[nt][2 * half] * f, acc[nt][2 * half + 1] * f);
         }
-        if (warp == 0 && tig == 0 && r < hvalid)
+        if (warp == 0 && tig == 0)
           p.lse[t * H + h0 + r] = live ? (m2 + log2f(l2)) * kLn2 : -INFINITY;
       }
       __syncthreads();
