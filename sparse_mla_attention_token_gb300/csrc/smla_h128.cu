@@ -515,7 +515,13 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   int ring_j[kRing];
   uint32_t ring_tok[kRing];
 
-  long long last = clock64();
+  // inputs already seen ready for the next P.V / the next S: none of them can
+  // complete another phase before that operation issues, so they are polled
+  // until seen once (every poll is a shared-memory access behind the
+  // producers' and score warps' traffic)
+  bool p_ok = false, kv_ok = false, sf_ok = false;
+  uint32_t idle = 0;          // passes since the last progress
+  long long last = 0;
   while (true) {
     bool progress = false;
     // ---- the next token's Q (gates its first S): ahead of a ready P.V
@@ -560,8 +566,8 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
     if (pg < sg) {
       const int jj = ring_j[pg % kRing];
       const uint32_t tk = ring_tok[pg % kRing];
-      if (mbar_test_wait(bar_addr(b->p_full[pg % kPBufs]), (pg / kPBufs) & 1) &&
-          (jj != 0 || mbar_test_wait(bar_addr(b->o_free), (tk & 1) ^ 1))) {
+      if (!p_ok) p_ok = mbar_test_wait(bar_addr(b->p_full[pg % kPBufs]), (pg / kPBufs) & 1);
+      if (p_ok && (jj != 0 || mbar_test_wait(bar_addr(b->o_free), (tk & 1) ^ 1))) {
         SMLA_TL(1, pg, 3);
         tc_fence_after();
         const uint32_t s = pg % kStages;
@@ -576,11 +582,13 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
         mma_commit(bar_addr(b->pv_done[pg % kPBufs]));
         SMLA_TL(1, pg, 4);
         ++pg;
+        p_ok = false;
         progress = true;
       }
     }
-    // ---- next S (walking tokens; tokens without valid slots have no tiles)
-    if (!progress && tok < p.T && sg - pg < kRing) {
+    // ---- next S (walking tokens; tokens without valid slots have no tiles), in
+    // the same pass as a P.V issued above (P.V still goes first)
+    if (tok < p.T && sg - pg < kRing) {
       if (!have_meta) {
         const int slot = it & 1;
         if (mbar_test_wait(bar_addr(b->meta_full[slot]), (it >> 1) & 1)) {
@@ -602,10 +610,13 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
       } else {
         const uint32_t s = sg % kStages, ph = (sg / kStages) & 1;
         const uint32_t sb = sg % kSBufs;
-        // the S buffer's previous tile, S(sg - kSBufs), has been read
-        if (mbar_test_wait(bar_addr(b->kv_full[s]), ph) &&
-            (sg < kSBufs ||
-             mbar_test_wait(bar_addr(b->s_free[(sg - kSBufs) & 1]), ((sg - kSBufs) >> 1) & 1))) {
+        // the tile has landed and the S buffer's previous tile, S(sg - kSBufs), has been read
+        if (!kv_ok) kv_ok = mbar_test_wait(bar_addr(b->kv_full[s]), ph);
+        if (kv_ok && !sf_ok)
+          sf_ok = sg < kSBufs ||
+                  mbar_test_wait(bar_addr(b->s_free[(sg - kSBufs) & 1]), ((sg - kSBufs) >> 1) & 1);
+        if (kv_ok && sf_ok) {
+          kv_ok = sf_ok = false;
           SMLA_TL(1, sg, 1);
           tc_fence_after();
           // K rows as K-major B (64-column blocks 8 KB apart); a K step of 16 elements is
@@ -640,17 +651,19 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
       }
     }
     if (tok >= p.T && pg == sg) break;   // every S and every P.V issued
+    // keep polling without a sleep: the next MMA issues as soon as its inputs are
+    // ready (a 32 ns sleep here cost 1-2%); the abort flag and the no-progress
+    // timer are looked at every 16th idle pass
     if (progress) {
-      last = clock64();
-    } else {
+      idle = 0;
+    } else if ((++idle & 15u) == 0) {
+      if (idle == 16) last = clock64();   // the idle stretch's first look
       if (*reinterpret_cast<volatile int*>(&b->abort_flag)) break;
       if (clock64() - last > kTimeoutCycles) {
         *reinterpret_cast<volatile int*>(&b->abort_flag) = 1;
         atomicOr(p.err, 2u);
         break;
       }
-      // keep polling without a sleep: the next MMA issues as soon as its inputs
-      // are ready (a 32 ns sleep here cost 1-2%)
     }
   }
   // drain: every MMA and copy issued must complete before TMEM is freed, and
