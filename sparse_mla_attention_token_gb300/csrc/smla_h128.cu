@@ -493,7 +493,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTileN, false, false);
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, 256, false, true);
-  constexpr int kRing = 8;   // issued-S tiles awaiting their P.V (at most kSBufs + 2)
+  constexpr int kRing = 8;   // issued-S tiles awaiting their P.V (at most kSBufs + 2; < 32 bits)
   // Operand descriptors are built once and advanced by adding (byte offset / 16)
   // to their start-address field (shared addresses < 256 KB: no carry out of it):
   // a thread issuing tcgen05.mma back to back is bound by its own issue path.
@@ -512,8 +512,9 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
   uint32_t sg = 0;            // next S tile (global)
   // P.V side
   uint32_t pg = 0;            // next P.V tile (global)
-  int ring_j[kRing];
-  uint32_t ring_tok[kRing];
+  // per issued S awaiting its P.V, bit (g mod 32): the tile is its token's first /
+  // its token's index is odd (registers, not a dynamically indexed local array)
+  uint32_t first_bits = 0, todd_bits = 0;
 
   // inputs already seen ready for the next P.V / the next S: none of them can
   // complete another phase before that operation issues, so they are polled
@@ -564,10 +565,10 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
     }
     // ---- next P.V
     if (pg < sg) {
-      const int jj = ring_j[pg % kRing];
-      const uint32_t tk = ring_tok[pg % kRing];
+      const uint32_t bit = 1u << (pg & 31u);
+      const bool first = (first_bits & bit) != 0;
       if (!p_ok) p_ok = mbar_test_wait(bar_addr(b->p_full[pg % kPBufs]), (pg / kPBufs) & 1);
-      if (p_ok && (jj != 0 || mbar_test_wait(bar_addr(b->o_free), (tk & 1) ^ 1))) {
+      if (p_ok && (!first || mbar_test_wait(bar_addr(b->o_free), ((todd_bits & bit) ? 1u : 0u) ^ 1u))) {
         SMLA_TL(1, pg, 3);
         tc_fence_after();
         const uint32_t s = pg % kStages;
@@ -575,7 +576,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
         // V as MN-major B: 64-column blocks 8 KB apart, 8-slot groups 1 KB apart; a K
         // step is 16 slot rows (2 KB = 128 in the descriptor's start-address field)
         const uint64_t vd = d_v0 + s * (kStageBytes >> 4);
-        mma_bf16_ts(tmem, ptm, vd, kIdescO, jj > 0 ? 1u : 0u);
+        mma_bf16_ts(tmem, ptm, vd, kIdescO, first ? 0u : 1u);
 #pragma unroll
         for (int kk = 1; kk < kTileN / 16; ++kk) mma_bf16_ts(tmem, ptm + kk * 8, vd + kk * 128, kIdescO, 1u);
         mma_commit(bar_addr(b->kv_empty[s]));
@@ -635,8 +636,11 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
           }
           mma_commit(bar_addr(b->s_full[sg & 1]));
           SMLA_TL(1, sg, 0);
-          ring_j[sg % kRing] = j;
-          ring_tok[sg % kRing] = tokn;
+          {
+            const uint32_t bit = 1u << (sg & 31u);
+            first_bits = j == 0 ? (first_bits | bit) : (first_bits & ~bit);
+            todd_bits = (tokn & 1u) ? (todd_bits | bit) : (todd_bits & ~bit);
+          }
           ++sg;
           progress = true;
           if (++j == nt) {   // the token's last S: its Q may be replaced
