@@ -535,8 +535,7 @@ __device__ void mma_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t t
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            tmem_cp_128x256b(tmem + kTmemQ + 8 * kk,
-                             sdesc_sw128(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024));
+            tmem_cp_128x256b(tmem + kTmemQ + 8 * kk, d_q0 + (kk >> 2) * 1024 + (kk & 3) * 2);
           mma_commit(bar_addr(b->qcp_done));
           q_state = 1;
           progress = true;
