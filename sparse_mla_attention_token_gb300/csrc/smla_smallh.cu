@@ -13,8 +13,10 @@
 //     rows are compacted, in slot order, into a shared-memory row list;
 //     invalid slots are never read (PR #6002 "Invalid KV rows");
 //   * rows are gathered 32 per tile with 16-byte cp.async into a two-stage
-//     ring (the next tile lands while this one is computed); the ragged tail
-//     of the last tile is zero-filled, so no pad row can inject NaN;
+//     ring (the next tile lands while this one is computed), each warp the
+//     64 columns it reads, so that (bf16) a warp waits for its own copies
+//     only; the ragged tail of the last tile is zero-filled, so no pad row
+//     can inject NaN;
 //   * M = 16 heads is below tcgen05's smallest tile (M = 64), so the two
 //     contractions use warp-level mma.sync m16n8k16 (bf16 in, fp32 out):
 //     the 8 warps split the 512-wide head dim, each owning 64 columns of
@@ -38,9 +40,11 @@
 //
 // fp8 cache (kFp8, 512 columns): each kv row is 512 e4m3 bytes and 4 fp32
 // scales, one per 128-column block (value = code * scale).  The gather moves
-// the 512 + 16 bytes with cp.async into an fp8 ring; at the start of each tile
-// the CTA decodes the codes exactly into the bf16 stage (e4m3 is a subset of
-// bf16); the scales are applied in fp32: to each warp's partial scores (a warp's
+// the 512 + 16 bytes with cp.async into an fp8 ring (16-byte chunk c of row r
+// at chunk c ^ 4 (r & 7), so that a warp's reads of 8 rows x 64 bytes spread
+// over the banks); at the start of each tile every warp decodes the codes of
+// its own 64 columns exactly into the bf16 stage (e4m3 is a subset of bf16)
+// behind a warp-level sync; the scales are applied in fp32: to each warp's partial scores (a warp's
 // 64 columns lie in one block) and to the probabilities, one bf16 copy of P per
 // block, so that P.V and the scores see code * scale without a second rounding
 // of the values.
@@ -224,8 +228,8 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
         const int slot = tile * kBN + r;
         const bool ok = slot < nvalid;
         const int64_t row = ok ? rows[slot] : 0;
-        if (c < 32)
-          cp_async_16(f0 + r * 512 + c * 16, cb + row * 512 + c * 16, ok ? 16u : 0u);
+        if (c < 32)   // chunk c at c ^ 4(r & 7): a warp's decode reads of 8 rows x 64 B spread over the banks
+          cp_async_16(f0 + r * 512 + ((c ^ ((r & 7) << 2)) << 4), cb + row * 512 + c * 16, ok ? 16u : 0u);
         else
           cp_async_16(s0 + r * 16, sb + row * 16, ok ? 16u : 0u);
       }
@@ -233,11 +237,12 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
       return;
     }
     const uint32_t dst0 = smem_u32(sm.kv[stage]);
-    constexpr int kChunks = kRowBytes / 16;   // 16-byte chunks per gathered row
-#pragma unroll 4
-    for (int i = tid; i < kBN * kChunks; i += kThreads) {
-      // non-negative: unsigned division (a shift and a mask for 64 chunks a row)
-      const int r = static_cast<int>(unsigned(i) / kChunks), c = static_cast<int>(unsigned(i) % kChunks);
+    // each warp copies its own 64 columns of the tile's rows (the only ones it
+    // reads: its score slice and its value columns), 8 lanes per 128-byte row
+    // piece, so a warp waits for its own copies alone
+#pragma unroll
+    for (int k = 0; k < kBN / 4; ++k) {
+      const int r = (lane >> 3) + 4 * k, c = warp * 8 + (lane & 7);
       const int slot = tile * kBN + r;
       const bool ok = slot < nvalid;
       const char* src = ok ? kvb + int64_t(rows[slot]) * kRowBytes + c * 16 : kvb;
@@ -292,8 +297,17 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
     for (int it = 0; it < ntiles; ++it, ++gt) {
       const int stage = gt & 1;
       cp_async_wait<0>();
-      __syncthreads();  // tile `it` landed; every warp is done with the other stage
+      // tile `it` landed.  bf16: a warp gathered, and reads, its own columns only,
+      // so its own copies and a warp-level sync suffice (it is also done with its
+      // columns of the other stage); fp8: the scales of every row are read by every
+      // warp before the next block barrier
+      if constexpr (kFp8) __syncthreads(); else __syncwarp();
       if (it + 1 < ntiles) {
+        // bf16: tile 1 goes into the stage the previous token's epilogue staged its
+        // output in; every warp must have copied that out first (other gathers into
+        // it follow a compaction, whose block barriers order them)
+        if constexpr (!kFp8)
+          if (it == 0) __syncthreads();
         issue_tile(t, cur, nv_cur, it + 1, stage ^ 1);
       } else if (tn < p.T) {
         nv_next = compact(tn, cur ^ 1);
@@ -301,13 +315,16 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
         if (nv_next > 0) issue_tile(tn, cur ^ 1, nv_next, 0, stage ^ 1);
       }
       if constexpr (kFp8) {
-        // decode the tile's e4m3 codes exactly into the bf16 stage (4 x 16 codes
-        // per thread); every warp finished the previous tile's P.V (barrier above)
+        // decode the tile's e4m3 codes exactly into the bf16 stage: each warp only
+        // its own 64 columns (the only ones it reads, for its score slice and for
+        // its value columns), so a warp-level sync is enough; the barrier above
+        // ordered the stage's previous readers (the output copy included)
+        static_assert(kDqk == 512 && kDv == 512 && Dm::kVWarps == kWarps, "fp8: 64 columns per warp");
         const uint32_t kv0 = smem_u32(sm.kv[0]);
 #pragma unroll
-        for (int k = 0; k < kBN * 32 / kThreads; ++k) {
-          const int i = tid + k * kThreads, r = i >> 5, c = i & 31;
-          const uint4 raw = *reinterpret_cast<const uint4*>(&sm.f8[stage][r * 512 + c * 16]);
+        for (int k = 0; k < kBN * 4 / 32; ++k) {
+          const int i = lane + k * 32, r = i >> 2, c = warp * 4 + (i & 3);
+          const uint4 raw = *reinterpret_cast<const uint4*>(&sm.f8[stage][r * 512 + ((c ^ ((r & 7) << 2)) << 4)]);
           const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t o[8];
 #pragma unroll
@@ -321,7 +338,7 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
           sts_u4(kv_chunk(kv0, r, 2 * c), make_uint4(o[0], o[1], o[2], o[3]));
           sts_u4(kv_chunk(kv0, r, 2 * c + 1), make_uint4(o[4], o[5], o[6], o[7]));
         }
-        __syncthreads();
+        __syncwarp();
       }
       const uint32_t kvs = smem_u32(sm.kv[kFp8 ? 0 : stage]);
       // ---- 3. partial S over this warp's 64 columns
