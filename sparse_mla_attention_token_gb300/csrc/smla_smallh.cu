@@ -115,9 +115,15 @@ struct __align__(128) Smem<512, 512, true> {
   int rows[2][kSmallHMaxSlots];
   int warp_cnt[Dm::kWarps];
   uint8_t f8[2][kBN * 512];                // fp8 ring: raw e4m3 rows
-  float scl[2][kBN][4];                    // their block scales
+  float scl[2][Dm::kWarps][kBN];           // per warp: its 128-column block's scale of each row
   static_assert(sizeof(kv[0]) >= kHG * Dm::kOStride * 2, "output staging fits one stage");
 };
+
+// 4-byte async copy global -> shared; src_bytes = 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
 
 template <int kRowBytes>
 __device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t base, int r, int c) {
@@ -218,20 +224,27 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
   auto issue_tile = [&](int64_t t, int buf, int nvalid, int tile, int stage) {
     const int* rows = sm.rows[buf];
     if constexpr (kFp8) {
-      // 32 chunks of codes and one chunk of scales per row; the tail zero-filled
-      const uint32_t f0 = smem_u32(sm.f8[stage]), s0 = smem_u32(sm.scl[stage]);
+      // each warp copies the codes of its own 64 columns (4 chunks of each row; chunk
+      // c at c ^ 4(r & 7), so that its decode reads of 8 rows x 64 B spread over the
+      // banks) and its 128-column block's scale of each row: all a warp reads before
+      // the next block barrier.  The tail is zero-filled.
+      static_assert(kBN == 32, "one row per lane for the scales");
+      const uint32_t f0 = smem_u32(sm.f8[stage]), s0 = smem_u32(&sm.scl[stage][warp][0]);
       const uint8_t* cb = static_cast<const uint8_t*>(p.kv);
       const char* sb = reinterpret_cast<const char*>(p.kv_scale);
-#pragma unroll 4
-      for (int i = tid; i < kBN * 33; i += kThreads) {
-        const int r = static_cast<int>(unsigned(i) / 33u), c = static_cast<int>(unsigned(i) % 33u);
+#pragma unroll
+      for (int k = 0; k < kBN / 8; ++k) {
+        const int r = (lane >> 2) + 8 * k, c = warp * 4 + (lane & 3);
         const int slot = tile * kBN + r;
         const bool ok = slot < nvalid;
         const int64_t row = ok ? rows[slot] : 0;
-        if (c < 32)   // chunk c at c ^ 4(r & 7): a warp's decode reads of 8 rows x 64 B spread over the banks
-          cp_async_16(f0 + r * 512 + ((c ^ ((r & 7) << 2)) << 4), cb + row * 512 + c * 16, ok ? 16u : 0u);
-        else
-          cp_async_16(s0 + r * 16, sb + row * 16, ok ? 16u : 0u);
+        cp_async_16(f0 + r * 512 + ((c ^ ((r & 7) << 2)) << 4), cb + row * 512 + c * 16, ok ? 16u : 0u);
+      }
+      {
+        const int slot = tile * kBN + lane;
+        const bool ok = slot < nvalid;
+        const int64_t row = ok ? rows[slot] : 0;
+        cp_async_4(s0 + lane * 4, sb + row * 16 + (warp >> 1) * 4, ok ? 4u : 0u);
       }
       cp_async_commit();
       return;
@@ -297,11 +310,16 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
     for (int it = 0; it < ntiles; ++it, ++gt) {
       const int stage = gt & 1;
       cp_async_wait<0>();
-      // tile `it` landed.  bf16: a warp gathered, and reads, its own columns only,
-      // so its own copies and a warp-level sync suffice (it is also done with its
-      // columns of the other stage); fp8: the scales of every row are read by every
-      // warp before the next block barrier
-      if constexpr (kFp8) __syncthreads(); else __syncwarp();
+      // tile `it` landed: a warp gathered, and reads before the next block barrier,
+      // its own columns (and, fp8, its own block's scales) only, so its own copies
+      // and a warp-level sync suffice; it is also done with its part of the other
+      // stage.  fp8: the decode stage also holds the previous token's staged
+      // output, which every warp must have copied out before a token's first decode.
+      if constexpr (kFp8) {
+        if (it == 0) __syncthreads(); else __syncwarp();
+      } else {
+        __syncwarp();
+      }
       if (it + 1 < ntiles) {
         // bf16: tile 1 goes into the stage the previous token's epilogue staged its
         // output in; every warp must have copied that out first (other gathers into
@@ -361,8 +379,8 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
         // this warp's 64 columns lie in scale block warp / 2: scale each slot's partial
   #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          const float c0 = sm.scl[stage][nt * 8 + 2 * tig][warp >> 1];
-          const float c1 = sm.scl[stage][nt * 8 + 2 * tig + 1][warp >> 1];
+          const float c0 = sm.scl[stage][warp][nt * 8 + 2 * tig];
+          const float c1 = sm.scl[stage][warp][nt * 8 + 2 * tig + 1];
           s[nt][0] *= c0; s[nt][1] *= c1; s[nt][2] *= c0; s[nt][3] *= c1;
         }
       }
@@ -430,7 +448,7 @@ __global__ void __launch_bounds__(Dims<kDqk, kDv>::kThreads, Dims<kDqk, kDv>::kM
   #pragma unroll
             for (int k = 0; k < kCols; k += 2)
               *reinterpret_cast<uint32_t*>(&sm.p[b][srow * kPStride + sc0 + k]) =
-                  pack_bf16x2(x[k] * sm.scl[stage][sc0 + k][b], x[k + 1] * sm.scl[stage][sc0 + k + 1][b]);
+                  pack_bf16x2(x[k] * sm.scl[stage][2 * b][sc0 + k], x[k + 1] * sm.scl[stage][2 * b][sc0 + k + 1]);
         } else {
   #pragma unroll
           for (int k = 0; k < kCols; k += 2)
