@@ -139,16 +139,20 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
       wait_tc(bar_addr_tc(b->full[c % kStagesTc]), (c / kStagesTc) & 1, b, true);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(kM, kNh, false, true);
+    // descriptors advanced from two built before the loop (byte offset / 16 added to
+    // the start-address field; shared addresses < 256 KB, so nothing carries out)
+    const uint64_t d_a0 = sdesc_sw128(sbase, 16, 1024);               // K-major A
+    const uint64_t d_b0 = sdesc_sw128(sbase + kABytes, 8192, 1024);   // MN-major B
     bool ok = true;
     for (int c = 0; c < kChunks && ok; ++c) {
       const int s = c % kStagesTc;
       if (!(ok = wait_tc(bar_addr_tc(b->full[s]), (c / kStagesTc) & 1, b, false))) break;
       tc_fence_after();
-      const uint32_t st = sbase + s * kStageBytesTc;
+      const uint64_t so = s * (kStageBytesTc >> 4);
 #pragma unroll
       for (int kk = 0; kk < kKc / 16; ++kk) {
-        const uint64_t ad = sdesc_sw128(st + kk * 32, 16, 1024);                 // K-major A
-        const uint64_t bd = sdesc_sw128(st + kABytes + kk * 16 * 128, 8192, 1024);  // MN-major B
+        const uint64_t ad = d_a0 + so + kk * 2;            // + kk * 32 bytes
+        const uint64_t bd = d_b0 + so + kk * (16 * 128 >> 4);   // + kk * 16 rows of 128 bytes
         mma_bf16_ss(tmem, ad, bd, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
       }
       mma_commit(bar_addr_tc(b->empty[s]));
@@ -558,6 +562,7 @@ __global__ void __launch_bounds__(kSdThreads, 2)
     cp_async_wait<0>();
   } else if (lane == 0) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(kSdM, kH, false, false);
+    const uint64_t d_sd0 = sdesc_sw128(sbase, 16, 1024);   // stage 0, K-major, 128-byte rows
     const int qrow = static_cast<int>(t * kH);
     bool ok = true;
     uint32_t loaded = 0;
@@ -576,12 +581,14 @@ __global__ void __launch_bounds__(kSdThreads, 2)
       if (!(ok = wait_sd(bar_addr_tc(b->full[s]), (c >> 1) & 1, b, false))) break;
       if (!(ok = wait_sd(bar_addr_tc(b->tma[s]), (c >> 1) & 1, b, false))) break;
       tc_fence_after();
-      const uint32_t st = sbase + s * kSdStage;
+      // descriptors advanced from one built before the loop (byte offset / 16 added to
+      // the start-address field; shared addresses < 256 KB, so nothing carries out)
+      const uint64_t da = d_sd0 + s * (kSdStage >> 4);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = sdesc_sw128(st + kk * 32, 16, 1024);
-        const uint64_t bq = sdesc_sw128(st + kSdA + kk * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(st + kSdA + kSdB + kk * 32, 16, 1024);
+        const uint64_t ad = da + kk * 2;
+        const uint64_t bq = da + (kSdA >> 4) + kk * 2;
+        const uint64_t bd = da + ((kSdA + kSdB) >> 4) + kk * 2;
         const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
         mma_bf16_ss(tmem, ad, bq, kIdesc, acc);            // S^T
         mma_bf16_ss(tmem + kH, ad, bd, kIdesc, acc);       // dP^T
