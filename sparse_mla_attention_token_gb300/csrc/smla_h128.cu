@@ -236,11 +236,22 @@ __device__ __forceinline__ int compact_token(const H128Params& p, int64_t tok, i
   return nv;
 }
 
-// This thread's cp.async copies of a tile have landed (wait_group): make them
-// visible to the tensor core's async proxy, then count them on the barrier.
-__device__ __forceinline__ void land_and_arrive(uint32_t bar) {
+// One arrive per warp on a barrier that counts warps: the warp-level sync orders
+// every lane's prior accesses (each lane fences its own first where a proxy or
+// tcgen05 ordering needs it) before lane 0's release arrive.  Warp-collective.
+// Per-thread arrives (224 a tile from the producers, 128 from a score warpgroup)
+// all update one barrier word; one per warp measured 1% faster on the kernel.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// This warp's cp.async copies of a tile have landed (wait_group in every lane):
+// each lane makes its own visible to the tensor core's async proxy, then the warp
+// counts them on the barrier.
+__device__ __forceinline__ void land_and_arrive(uint32_t bar, int lane) {
   fence_proxy_async_smem();
-  mbar_arrive(bar);
+  warp_arrive(bar, lane);
 }
 
 // Warps 0-6 gather every tile together: warp w copies rows w, w+7, ... (lane c
@@ -341,7 +352,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
       put(cc, w16, cc - kHeld);
     }
     tc_fence_before();
-    mbar_arrive(bar_addr(b->o_free));   // all of O has been read
+    warp_arrive(bar_addr(b->o_free), lane);   // all of O has been read
 #pragma unroll
     for (int cc = 0; cc < kHeld; ++cc) put(cc, held[cc], 8 - kHeld + cc);
     if (lane == 0) SMLA_TL(3, ep_gl, 6);
@@ -452,7 +463,7 @@ __device__ void producer_role(const H128Params& p, const CUtensorMap* tm_q, cons
         // slowest warp, so counting it after the next tile's issue (overlapping
         // the two) made every tile ready later (2% slower overall)
         cp_async_wait<0>();
-        land_and_arrive(bar_addr(b->kv_full[s]));
+        land_and_arrive(bar_addr(b->kv_full[s]), lane);
         if (lane == 0) SMLA_TL(0, g, 2);
         if (!compacted && j == ntiles - 1) compact_next();   // after counting the tile
       }
@@ -754,7 +765,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
                                                  b, p.err, 4u));
     if (!ok) break;
     const int nv = b->nvalid[slot];
-    mbar_arrive(bar_addr(b->meta_empty[slot]));
+    warp_arrive(bar_addr(b->meta_empty[slot]), lane);
     if (nv == 0) continue;   // written by the producer warps
     const int ntiles = (nv + kTileN - 1) / kTileN;
     float l_w = 0.f, m_lw = -INFINITY;   // this warpgroup's sum and the max it is relative to
@@ -778,7 +789,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
         tmem_ld32(tl + kTmemS + sb * kTileN + 32, sv + 32);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar_addr(b->s_free[g & 1]));
+        warp_arrive(bar_addr(b->s_free[g & 1]), lane);
         // the row's top partial in base-2 logits over the valid columns (rounding
         // is monotone, so the extreme raw value scales to the largest scaled one;
         // a negative scale turns the smallest raw value into it).  The zero-filled
@@ -861,7 +872,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
       const bool need = mx > m_prev + 8.f;
       const float m_new = need ? mx : m_prev;
       m_sh[(g & 1) * 128 + row] = m_new;
-      mbar_arrive(bar_addr(b->m_ready[g & 1][qd]));
+      warp_arrive(bar_addr(b->m_ready[g & 1][qd]), lane);
       if (row == 0) SMLA_TL(2, g, 3);
       // 5. P = 2^(S - m), this warpgroup's sum (s holds S - off)
       const float m_rel = m_new - off;
@@ -914,7 +925,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_addr(b->p_full[pb]));
+      warp_arrive(bar_addr(b->p_full[pb]), lane);
       // receive buffer xb may be refilled: every lane's reads of it were consumed above
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer[xb]);
@@ -926,7 +937,7 @@ __device__ void score_role(const H128Params& p, uint8_t* base, Bars* b, uint32_t
     float* lsh = l_sh + (et & 1) * 512;
     lsh[wg * 256 + row] = l_w;
     lsh[wg * 256 + 128 + row] = m_lw;
-    mbar_arrive(bar_addr(b->epi[et & 1]));
+    warp_arrive(bar_addr(b->epi[et & 1]), lane);
     ++et;
   }
 }
@@ -947,29 +958,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(b->qcp_done), 1);
     mbar_init(bar_addr(b->q_empty), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_addr(b->kv_full[s]), kProducerThreads);
+      mbar_init(bar_addr(b->kv_full[s]), kProducerWarps);
       mbar_init(bar_addr(b->kv_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->s_full[i]), 1);
-      mbar_init(bar_addr(b->s_free[i]), kWgThreads);
+      mbar_init(bar_addr(b->s_free[i]), kWgThreads / 32);
     }
     for (int i = 0; i < 2; ++i)
-      for (int q = 0; q < 4; ++q) mbar_init(bar_addr(b->m_ready[i][q]), 32);
-    for (int i = 0; i < 2; ++i) mbar_init(bar_addr(b->epi[i]), 2 * kWgThreads);
+      for (int q = 0; q < 4; ++q) mbar_init(bar_addr(b->m_ready[i][q]), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(bar_addr(b->epi[i]), 2 * kWgThreads / 32);
     for (int i = 0; i < kPBufs; ++i) {
-      mbar_init(bar_addr(b->p_full[i]), kWgThreads);
+      mbar_init(bar_addr(b->p_full[i]), kWgThreads / 32);
       mbar_init(bar_addr(b->pv_done[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(b->meta_full[i]), 1);
-      mbar_init(bar_addr(b->meta_empty[i]), 1 + 2 * kWgThreads);
+      mbar_init(bar_addr(b->meta_empty[i]), 1 + 2 * kWgThreads / 32);
     }
     for (int i = 0; i < kXBufs; ++i) {
       mbar_init(bar_addr(b->x_full[i]), 1);     // local expect_tx + the peer's st.async bytes
       mbar_init(bar_addr(b->x_free[i]), 4);     // one arrive per peer swap warp
     }
-    mbar_init(bar_addr(b->o_free), 128);   // producer warps 0-3 after the epilogue
+    mbar_init(bar_addr(b->o_free), 4);     // producer warps 0-3 after the epilogue
     mbar_init(bar_addr(b->drain), 1);
     b->abort_flag = 0;
     b->prod_stop = 0;
