@@ -71,6 +71,20 @@ def test_fp8_variants(B, variant):
     _run(B, x, kv8, sc)
 
 
+@pytest.mark.parametrize("H", [8, 16])
+def test_fp8_token_mix_per_cta(B, H):
+    # Several tokens per CTA with valid counts rotating through none, one tile, a
+    # tile and one slot, two and three tiles: each warp gathers, decodes and scales
+    # its own columns (its block's scales in its own slot) and a token's first tile
+    # waits for the previous token's staged output to be copied out.
+    cfg = synth.CONFIGS["tiny"].with_(T=1400, H=H, pool=400, ratio=1, topk=96, window=64,
+                                      seed=430 + H)
+    x = synth.make_inputs(cfg)
+    keep = np.array([0, 20, 32, 33, 64, 70, 96])[np.arange(cfg.T) % 7]
+    x["idx"][np.arange(cfg.topk)[None, :] >= keep[:, None]] = -1
+    _run(B, x, *synth.fp8_cache(x["kv"]))
+
+
 @pytest.mark.parametrize("variant", ["wide_scales", "wide_scales_t4", "big_q", "tiny_q"])
 def test_fp8_value_ranges(B, variant):
     # the fp16 operands' range handling: Q far outside fp16's range either way (the

@@ -223,6 +223,26 @@ def test_tokens_pipelined_per_cta(B, H, idx64):
     compare(out, lse, O, L)
 
 
+@pytest.mark.parametrize("H", [8, 16])
+def test_small_head_token_mix_per_cta(B, H):
+    # Each small-head CTA walks several tokens whose valid counts rotate through
+    # none, one tile, a tile and one slot, two tiles and three tiles: a warp gathers
+    # and reads only its own columns, so a tile starts on a warp-level sync, and a
+    # token's second tile goes into the stage the previous token staged its output
+    # in (ordered by one block barrier).  H = 8 also exercises the warps whose rows
+    # are all past the head count.
+    cfg = synth.CONFIGS["tiny"].with_(T=1400, H=H, pool=400, ratio=1, topk=96, window=64,
+                                      seed=23 + H)
+    x = synth.make_inputs(cfg)
+    idx = x["idx"].copy()
+    keep = np.array([0, 20, 32, 33, 64, 70, 96])[np.arange(cfg.T) % 7]
+    idx[np.arange(cfg.topk)[None, :] >= keep[:, None]] = -1
+    x["idx"] = idx
+    out, lse, _ = _run(B, x)
+    O, L = orc.sparse_mla_fwd(x["q"], x["kv"], x["idx"], x["sink"], x["scale"])
+    compare(out, lse, O, L)
+
+
 @pytest.mark.parametrize("H", HEADS)
 @pytest.mark.parametrize("topk,window", [(1, 1), (3, 2), (67, 40), (130, 64), (2048, 150),
                                          (2500, 200)])
